@@ -1,0 +1,206 @@
+/*
+ * segtopk — segmented (batched) top-k by multi-pass radix digit selection,
+ * written for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI. All pointers are plain pointers; no C++ or framework types cross
+ * this boundary. Every call is asynchronous on the given CUDA stream unless
+ * its comment says otherwise.
+ *
+ * What is computed (per segment, independently):
+ *   "Implement Segmented TopK using Thread-Block-Clusters" (CUB pull request),
+ *   section 1 "High-level overview": for each of num_segments variable-length
+ *   segments select the k largest (or smallest) keys, optionally carrying a
+ *   value payload. The selection contract (which items, in which order) is
+ *   the one of the CUB documentation page "Top-K: Determinism, Tie-Breaking,
+ *   and Output Ordering" (sections "Requirements reference" and "Which items
+ *   are selected?"), with +0.0 and -0.0 ranked as equal keys whose own bit
+ *   patterns are written to the output ("Fix BlockTopK +/-0.0 handling",
+ *   sections Cause and Fix).
+ */
+#ifndef SEGTOPK_H_
+#define SEGTOPK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Key element types. Keys are read as raw bit patterns of this width. */
+typedef enum {
+  SEGTOPK_F16 = 0,  /* IEEE binary16 */
+  SEGTOPK_BF16 = 1, /* bfloat16 */
+  SEGTOPK_F32 = 2,  /* IEEE binary32 */
+  SEGTOPK_F64 = 3,  /* IEEE binary64 */
+  SEGTOPK_U32 = 4,  /* uint32_t */
+  SEGTOPK_I32 = 5   /* int32_t */
+} segtopk_dtype;
+
+/* Which end of the order is selected (CUB's Max* / Min* entry points). */
+typedef enum { SEGTOPK_MAX = 0, SEGTOPK_MIN = 1 } segtopk_direction;
+
+/* Result-set reproducibility ("Top-K: Determinism, ...", "Determinism" table). */
+typedef enum {
+  SEGTOPK_NOT_GUARANTEED = 0,
+  SEGTOPK_RUN_TO_RUN = 1,
+  SEGTOPK_GPU_TO_GPU = 2
+} segtopk_determinism;
+
+/* Boundary tie policy (same page, "Tie-break" table). A concrete tie-break
+ * requires SEGTOPK_GPU_TO_GPU; UNSPECIFIED is resolved as
+ * PREFER_SMALLER_INDEX by this library in every determinism mode. */
+typedef enum {
+  SEGTOPK_TIE_UNSPECIFIED = 0,
+  SEGTOPK_PREFER_SMALLER_INDEX = 1,
+  SEGTOPK_PREFER_LARGER_INDEX = 2
+} segtopk_tie_break;
+
+/* Output order of the selected items (same page, "Output ordering" table).
+ * UNSORTED: any order (this library writes a fixed, repeatable order).
+ * SORTED: by key, better first; equal keys in unspecified order (this
+ *         library writes them in source-index order, i.e. as STABLE_SORTED).
+ * STABLE_SORTED: by key, better first; equal keys by source index ascending,
+ *         whatever the tie-break. */
+typedef enum {
+  SEGTOPK_UNSORTED = 0,
+  SEGTOPK_SORTED = 1,
+  SEGTOPK_STABLE_SORTED = 2
+} segtopk_ordering;
+
+/* Status codes returned by every entry point. */
+typedef enum {
+  SEGTOPK_SUCCESS = 0,
+  SEGTOPK_ERROR_INVALID_VALUE = 1,       /* bad enum, null pointer, negative size, k < 0 */
+  SEGTOPK_ERROR_INVALID_COMBINATION = 2, /* determinism / tie_break pair not allowed */
+  SEGTOPK_ERROR_NOT_SUPPORTED = 3,       /* size or k outside this library's limits */
+  SEGTOPK_ERROR_MISALIGNED = 4,          /* keys pointer not 16-byte aligned */
+  SEGTOPK_ERROR_CUDA = 5,                /* a CUDA runtime call failed: see segtopk_last_cuda_error */
+  SEGTOPK_ERROR_DEVICE = 6               /* current device is not an sm_103 GPU */
+} segtopk_status;
+
+/* Largest k this build serves (the selected items of one segment are held
+ * and sorted on chip). Calls with a larger k return SEGTOPK_ERROR_NOT_SUPPORTED
+ * unless every segment is no longer than k and the ordering is UNSORTED
+ * (then every key is selected and the call is a copy). */
+#define SEGTOPK_MAX_K 2048
+
+/* Largest segment length (keys) accepted: segment-local indices are 32-bit. */
+#define SEGTOPK_MAX_SEGMENT_LEN 2147483647LL
+
+/*
+ * Segmented top-k.
+ *
+ * Semantics: "Implement Segmented TopK using Thread-Block-Clusters", sections
+ * 1.2 "Radix (digit) top-k" (method), 1.5 "Final filter and output placement"
+ * and 1.6 "Determinism / tie-breaking"; contract of "Top-K: Determinism,
+ * Tie-Breaking, and Output Ordering"; +/-0.0 handling of "Fix BlockTopK
+ * +/-0.0 handling".
+ *
+ * Arguments (all device pointers unless stated):
+ *   key_dtype        element type of keys and out_keys.
+ *   keys             key array; segment s covers elements
+ *                    [segment_offsets[s], segment_offsets[s+1]). Must be
+ *                    16-byte aligned. Read only.
+ *   values           optional int32 payload parallel to keys (NULL: keys only).
+ *   segment_offsets  int64 array of num_segments + 1 element offsets. A
+ *                    segment whose end is not greater than its begin is empty.
+ *   num_segments     number of segments (>= 0).
+ *   k                items to select per segment (>= 0).
+ *   direction, determinism, tie_break, ordering: see the enums. Valid
+ *                    (determinism, tie_break) pairs: (any, UNSPECIFIED) and
+ *                    (GPU_TO_GPU, PREFER_SMALLER_INDEX | PREFER_LARGER_INDEX).
+ *   out_keys         num_segments * k elements; segment s writes slots
+ *                    [s*k, s*k + min(k, n_s)) with the original key bits and
+ *                    leaves [s*k + n_s, s*k + k) untouched when n_s < k.
+ *   out_values       num_segments * k int32; required iff values != NULL;
+ *                    out_values[j] = values[segment_offsets[s] + i] for the
+ *                    element i written to out_keys[j].
+ *   max_segment_len  host-side upper bound on every segment's length. A
+ *                    negative value means unknown: the library then copies
+ *                    segment_offsets to the host and waits for the stream
+ *                    (a synchronising call). A bound that is too small is a
+ *                    caller error: longer segments are left unwritten.
+ *   stream           cudaStream_t (NULL = the legacy default stream).
+ *
+ * Ownership: the caller owns every buffer. The library allocates no device
+ * memory; it caches device attributes and per-kernel shared-memory limits.
+ * Inputs must not overlap outputs.
+ *
+ * Errors: argument errors are detected on the host before any launch and
+ * nothing is launched. num_segments == 0 or k == 0 is a successful no-op.
+ * A failed launch returns SEGTOPK_ERROR_CUDA (segtopk_last_cuda_error()
+ * gives the cudaError_t). The call does not synchronise (except as noted
+ * for max_segment_len < 0).
+ */
+int segtopk_batched_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+                         const int64_t* segment_offsets, int64_t num_segments, int32_t k,
+                         segtopk_direction direction, segtopk_determinism determinism,
+                         segtopk_tie_break tie_break, segtopk_ordering ordering, void* out_keys,
+                         int32_t* out_values, int64_t max_segment_len, void* stream);
+
+/* Optional launch controls for segtopk_batched_topk_ex (zero = automatic). */
+typedef struct {
+  /* CTAs per segment: 0 chooses it from the occupancy the device reports
+   * (fewest waves, ties toward the widest cluster); 1..16 forces the width
+   * (widths above 8 need non-portable cluster support). */
+  int32_t cluster_width;
+  int32_t reserved[7]; /* must be zero */
+} segtopk_options;
+
+/* segtopk_batched_topk with launch controls; options may be NULL. Returns
+ * SEGTOPK_ERROR_INVALID_VALUE for a width outside 0..16 or nonzero reserved
+ * fields, and SEGTOPK_ERROR_NOT_SUPPORTED when the device cannot launch the
+ * requested width. */
+int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+                            const int64_t* segment_offsets, int64_t num_segments, int32_t k,
+                            segtopk_direction direction, segtopk_determinism determinism,
+                            segtopk_tie_break tie_break, segtopk_ordering ordering, void* out_keys,
+                            int32_t* out_values, int64_t max_segment_len,
+                            const segtopk_options* options, void* stream);
+
+/*
+ * Same operation with HOST buffers: keys, values, segment_offsets, out_keys
+ * and out_values are host pointers (pinned memory gives full copy
+ * bandwidth). The caller also passes a device workspace of at least
+ * segtopk_host_workspace_bytes(...) bytes (the library allocates nothing).
+ * The call copies the inputs to the device, runs segtopk_batched_topk on
+ * `stream`, copies the results back and waits for the stream before
+ * returning (so the host outputs are ready on return).
+ */
+int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+                              const int64_t* segment_offsets, int64_t num_segments, int32_t k,
+                              segtopk_direction direction, segtopk_determinism determinism,
+                              segtopk_tie_break tie_break, segtopk_ordering ordering,
+                              void* out_keys, int32_t* out_values, int64_t max_segment_len,
+                              void* device_workspace, size_t workspace_bytes, void* stream);
+
+/* Device workspace bytes segtopk_batched_topk_host needs for these sizes
+ * (num_keys = number of key elements the offsets address, i.e. the largest
+ * segment end). Host-only arithmetic. */
+size_t segtopk_host_workspace_bytes(segtopk_dtype key_dtype, int has_values, int64_t num_keys,
+                                    int64_t num_segments, int32_t k);
+
+/* Human-readable text of a status code (static storage). */
+const char* segtopk_status_string(int status);
+
+/* cudaError_t of the last SEGTOPK_ERROR_CUDA on the calling thread (0 if none). */
+int segtopk_last_cuda_error(void);
+
+/*
+ * Reads and clears the device-side error word of the current device. The
+ * kernels bound every wait on an asynchronous copy; a wait that gives up
+ * sets this word (bit 0: copy wait timed out; bit 1: a segment longer than
+ * the launch was planned for). Synchronises the device. Returns a status;
+ * the word is stored in *error_word.
+ */
+int segtopk_read_device_error(uint32_t* error_word);
+
+/* Number of kernel launches the last successful call on this thread made. */
+int segtopk_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SEGTOPK_H_ */

@@ -1,0 +1,188 @@
+"""ctypes binding of libsegtopk.so (argument marshalling only).
+
+Every step of the selection runs in the library's CUDA kernels; this module
+turns tensors into pointers and names into enum values. It never falls back
+to another implementation: if the library is missing, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+# Enum values of include/segtopk.h
+DTYPE = {"f16": 0, "bf16": 1, "f32": 2, "f64": 3, "u32": 4, "i32": 5}
+KEY_BYTES = {"f16": 2, "bf16": 2, "f32": 4, "f64": 8, "u32": 4, "i32": 4}
+DIRECTION = {"max": 0, "min": 1}
+DETERMINISM = {"not_guaranteed": 0, "run_to_run": 1, "gpu_to_gpu": 2}
+TIE_BREAK = {"unspecified": 0, "prefer_smaller_index": 1, "prefer_larger_index": 2}
+ORDERING = {"unsorted": 0, "sorted": 1, "stable_sorted": 2}
+STATUS = {0: "SUCCESS", 1: "INVALID_VALUE", 2: "INVALID_COMBINATION", 3: "NOT_SUPPORTED",
+          4: "MISALIGNED", 5: "CUDA", 6: "DEVICE"}
+MAX_K = 2048
+
+_TORCH_TO_DTYPE = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32",
+                   torch.float64: "f64", torch.int32: "i32"}
+if hasattr(torch, "uint32"):
+    _TORCH_TO_DTYPE[torch.uint32] = "u32"
+
+
+class SegTopKError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+
+
+class Options(ctypes.Structure):
+    _fields_ = [("cluster_width", ctypes.c_int32), ("reserved", ctypes.c_int32 * 7)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load libsegtopk.so (built by __graft_entry__.build() or _build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError("libsegtopk.so is not built (run __graft_entry__.build()); "
+                           "there is no fallback implementation")
+    L = ctypes.CDLL(path)
+    c_int, c_i32, c_i64, vp = ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    L.segtopk_batched_topk.restype = c_int
+    L.segtopk_batched_topk.argtypes = [c_int, vp, vp, vp, c_i64, c_i32, c_int, c_int, c_int, c_int,
+                                       vp, vp, c_i64, vp]
+    L.segtopk_batched_topk_ex.restype = c_int
+    L.segtopk_batched_topk_ex.argtypes = [c_int, vp, vp, vp, c_i64, c_i32, c_int, c_int, c_int, c_int,
+                                          vp, vp, c_i64, ctypes.POINTER(Options), vp]
+    L.segtopk_batched_topk_host.restype = c_int
+    L.segtopk_batched_topk_host.argtypes = [c_int, vp, vp, vp, c_i64, c_i32, c_int, c_int, c_int,
+                                            c_int, vp, vp, c_i64, vp, ctypes.c_size_t, vp]
+    L.segtopk_host_workspace_bytes.restype = ctypes.c_size_t
+    L.segtopk_host_workspace_bytes.argtypes = [c_int, c_int, c_i64, c_i64, c_i32]
+    L.segtopk_status_string.restype = ctypes.c_char_p
+    L.segtopk_status_string.argtypes = [c_int]
+    L.segtopk_last_cuda_error.restype = c_int
+    L.segtopk_last_cuda_error.argtypes = []
+    L.segtopk_last_launch_count.restype = c_int
+    L.segtopk_last_launch_count.argtypes = []
+    L.segtopk_read_device_error.restype = c_int
+    L.segtopk_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    _lib = L
+    return L
+
+
+def _check(rc: int):
+    if rc != 0:
+        L = load()
+        msg = L.segtopk_status_string(rc).decode()
+        if rc == 5:
+            msg += " (cudaError %d)" % L.segtopk_last_cuda_error()
+        raise SegTopKError(rc, "segtopk: " + msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def key_dtype_of(t: torch.Tensor, key_dtype: str | None) -> str:
+    if key_dtype is not None:
+        if t.element_size() != KEY_BYTES[key_dtype]:
+            raise ValueError("keys element size does not match key_dtype %s" % key_dtype)
+        return key_dtype
+    if t.dtype not in _TORCH_TO_DTYPE:
+        raise ValueError("cannot infer key type from %s; pass key_dtype" % t.dtype)
+    return _TORCH_TO_DTYPE[t.dtype]
+
+
+def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, values=None,
+                 direction: str = "max", determinism: str = "gpu_to_gpu",
+                 tie_break: str = "prefer_smaller_index", ordering: str = "stable_sorted",
+                 out_keys=None, out_values=None, max_segment_len: int | None = None,
+                 key_dtype: str | None = None, stream=None, cluster_width: int = 0):
+    """Segmented top-k on the GPU through libsegtopk (see include/segtopk.h).
+
+    keys: 1-D CUDA tensor (16-byte aligned); its element size must match the
+    key type (a raw-bits tensor of the same width works with key_dtype).
+    segment_offsets: int64 CUDA tensor of num_segments + 1 offsets.
+    Returns (out_keys, out_values) of shape [num_segments * k]; out_values is
+    None for keys-only calls. Slots past a short segment's length are left as
+    they were in the given out tensors (uninitialised if allocated here).
+    """
+    L = load()
+    kd = key_dtype_of(keys, key_dtype)
+    if segment_offsets.dtype != torch.int64:
+        raise ValueError("segment_offsets must be int64")
+    num_segments = segment_offsets.numel() - 1
+    if out_keys is None:
+        out_keys = torch.empty(max(num_segments, 0) * k, dtype=keys.dtype, device=keys.device)
+    if values is not None and out_values is None:
+        out_values = torch.empty(max(num_segments, 0) * k, dtype=torch.int32, device=keys.device)
+    ml = -1 if max_segment_len is None else int(max_segment_len)
+    opts = Options()
+    opts.cluster_width = int(cluster_width)
+    rc = L.segtopk_batched_topk_ex(DTYPE[kd], _ptr(keys), _ptr(values), _ptr(segment_offsets),
+                                   num_segments, int(k), DIRECTION[direction],
+                                   DETERMINISM[determinism], TIE_BREAK[tie_break], ORDERING[ordering],
+                                   _ptr(out_keys), _ptr(out_values), ml, ctypes.byref(opts),
+                                   _stream_handle(stream, keys.device))
+    _check(rc)
+    return out_keys, out_values
+
+
+def host_workspace_bytes(key_dtype: str, has_values: bool, num_keys: int, num_segments: int,
+                         k: int) -> int:
+    return int(load().segtopk_host_workspace_bytes(DTYPE[key_dtype], int(has_values), num_keys,
+                                                   num_segments, k))
+
+
+def batched_topk_host(key_dtype: str, keys: torch.Tensor, segment_offsets: torch.Tensor, k: int,
+                      workspace: torch.Tensor, *, values=None, direction: str = "max",
+                      determinism: str = "gpu_to_gpu", tie_break: str = "prefer_smaller_index",
+                      ordering: str = "stable_sorted", out_keys=None, out_values=None,
+                      max_segment_len: int | None = None, stream=None):
+    """Host-buffer variant: keys/values/offsets/outputs are CPU tensors
+    (pinned for full copy bandwidth); `workspace` is a CUDA byte tensor of at
+    least host_workspace_bytes(...) bytes. Synchronises before returning."""
+    L = load()
+    num_segments = segment_offsets.numel() - 1
+    if out_keys is None:
+        out_keys = torch.empty(num_segments * k, dtype=keys.dtype)
+    if values is not None and out_values is None:
+        out_values = torch.empty(num_segments * k, dtype=torch.int32)
+    ml = -1 if max_segment_len is None else int(max_segment_len)
+    rc = L.segtopk_batched_topk_host(DTYPE[key_dtype], _ptr(keys), _ptr(values), _ptr(segment_offsets),
+                                     num_segments, int(k), DIRECTION[direction],
+                                     DETERMINISM[determinism], TIE_BREAK[tie_break],
+                                     ORDERING[ordering], _ptr(out_keys), _ptr(out_values), ml,
+                                     _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                     _stream_handle(stream, workspace.device))
+    _check(rc)
+    return out_keys, out_values
+
+
+def read_device_error() -> int:
+    """Reads and clears the kernels' device error word (synchronises)."""
+    w = ctypes.c_uint32(0)
+    _check(load().segtopk_read_device_error(ctypes.byref(w)))
+    return int(w.value)
+
+
+def last_launch_count() -> int:
+    return int(load().segtopk_last_launch_count())

@@ -1,0 +1,419 @@
+// C ABI of the segmented top-k library: argument validation, launch planning
+// and dispatch to the per-key-type kernels. See include/segtopk.h.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/segtopk.h"
+#include "block_select.cuh"
+#include "dispatch.h"
+#include "stream_topk.cuh"
+
+namespace segtopk {
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+thread_local int t_last_launch_count = 0;
+
+int cuda_fail(cudaError_t e)
+{
+  t_last_cuda_error = (int)e;
+  return SEGTOPK_ERROR_CUDA;
+}
+
+const KeyOps* ops_for(int dtype)
+{
+  switch (dtype) {
+  case SEGTOPK_F16: return &key_ops_f16();
+  case SEGTOPK_BF16: return &key_ops_bf16();
+  case SEGTOPK_F32: return &key_ops_f32();
+  case SEGTOPK_F64: return &key_ops_f64();
+  case SEGTOPK_U32: return &key_ops_u32();
+  case SEGTOPK_I32: return &key_ops_i32();
+  default: return nullptr;
+  }
+}
+
+// Device facts, cached per device.
+struct DeviceInfo {
+  bool valid = false;
+  int major = 0, minor = 0, sms = 0;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+cudaError_t device_info(DeviceInfo* out)
+{
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return e;
+  if (dev < 0 || dev >= 64)
+    return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.valid) {
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return e;
+    if ((e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return e;
+    if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return e;
+    d.valid = true;
+  }
+  *out = d;
+  return cudaSuccess;
+}
+
+constexpr uint32_t kStages = 4;
+constexpr int64_t kMinSliceKeys = 16384; // a CTA of a multi-CTA cluster reads at least this many keys
+constexpr int kThreads = 256;
+
+struct Plan {
+  LaunchShape shape;
+  uint32_t list_cap;
+  uint32_t ring_bytes;
+};
+
+uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Shared-memory sizing for a given k and cluster width.
+Plan size_plan(const KeyOps& ops, int32_t k, int cluster)
+{
+  Plan pl;
+  const uint32_t kb = (uint32_t)ops.key_bytes;
+  const uint32_t chunk_keys = kChunkBytes / kb;
+  pl.list_cap = align_up((uint32_t)k + chunk_keys, 32);
+  // the ring doubles as sort scratch (and, in a cluster leader, as gather space)
+  uint32_t sort_need = sort_scratch_bytes((uint32_t)k, ops.rank_bits);
+  if (cluster > 1)
+    sort_need += align_up((uint32_t)k * kb, 16) + align_up((uint32_t)k * 4u, 16);
+  pl.ring_bytes = align_up(std::max(kStages * kChunkBytes, sort_need), 128);
+  uint32_t smem = kCtrlBytes + pl.ring_bytes + align_up(pl.list_cap * kb, 16) + pl.list_cap * 4u;
+  pl.shape.threads = kThreads;
+  pl.shape.cluster = cluster;
+  pl.shape.smem = smem;
+  return pl;
+}
+
+// Cluster width: fewest waves of resident clusters over all segments, ties
+// toward the widest cluster ("Implement Segmented TopK using
+// Thread-Block-Clusters", section 3.3 "Wave-aware cluster-size search"),
+// using the occupancy the device reports for this kernel and its
+// shared-memory size. A CTA of a multi-CTA cluster must get at least
+// kMinSliceKeys keys of the longest segment.
+cudaError_t choose_plan(const KeyOps& ops, int64_t num_segments, int64_t max_len, int32_t k, Plan* out)
+{
+  static const int widths[] = {1, 2, 3, 4, 6, 8, 12, 16};
+  bool have = false;
+  int64_t best_waves = 0;
+  for (int c : widths) {
+    if (c > 1 && max_len < (int64_t)c * kMinSliceKeys)
+      break;
+    Plan pl = size_plan(ops, k, c);
+    int resident = 0;
+    cudaError_t e = ops.occupancy(pl.shape, &resident);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError(); // an unlaunchable width is skipped, not an error
+      continue;
+    }
+    if (resident <= 0)
+      continue;
+    const int64_t waves = (num_segments + resident - 1) / resident;
+    if (!have || waves <= best_waves) {
+      have = true;
+      best_waves = waves;
+      *out = pl;
+    }
+  }
+  return have ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
+bool valid_pair(int det, int tie)
+{
+  if (tie == SEGTOPK_TIE_UNSPECIFIED)
+    return true;
+  return det == SEGTOPK_GPU_TO_GPU;
+}
+
+int validate(int dtype, const void* keys, const int32_t* values, const int64_t* offsets,
+             int64_t num_segments, int32_t k, int direction, int determinism, int tie_break,
+             int ordering, const void* out_keys, const int32_t* out_values, int64_t max_len)
+{
+  if (dtype < SEGTOPK_F16 || dtype > SEGTOPK_I32)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if (direction != SEGTOPK_MAX && direction != SEGTOPK_MIN)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if (determinism < SEGTOPK_NOT_GUARANTEED || determinism > SEGTOPK_GPU_TO_GPU)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if (tie_break < SEGTOPK_TIE_UNSPECIFIED || tie_break > SEGTOPK_PREFER_LARGER_INDEX)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if (ordering < SEGTOPK_UNSORTED || ordering > SEGTOPK_STABLE_SORTED)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if (!valid_pair(determinism, tie_break))
+    return SEGTOPK_ERROR_INVALID_COMBINATION;
+  if (num_segments < 0 || k < 0)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if (num_segments == 0 || k == 0)
+    return SEGTOPK_SUCCESS;
+  if (!keys || !offsets || !out_keys || (values && !out_values) || (!values && out_values))
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if (((uintptr_t)keys & 15u) != 0)
+    return SEGTOPK_ERROR_MISALIGNED;
+  if (max_len > SEGTOPK_MAX_SEGMENT_LEN)
+    return SEGTOPK_ERROR_NOT_SUPPORTED;
+  if (k > SEGTOPK_MAX_K)
+    return SEGTOPK_ERROR_NOT_SUPPORTED;
+  if (num_segments > (int64_t)0x7fffffff / 16)
+    return SEGTOPK_ERROR_NOT_SUPPORTED;
+  return -1; // proceed
+}
+
+} // namespace
+} // namespace segtopk
+
+using namespace segtopk;
+
+extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+                                       const int64_t* segment_offsets, int64_t num_segments, int32_t k,
+                                       segtopk_direction direction, segtopk_determinism determinism,
+                                       segtopk_tie_break tie_break, segtopk_ordering ordering,
+                                       void* out_keys, int32_t* out_values, int64_t max_segment_len,
+                                       const segtopk_options* options, void* stream)
+{
+  t_last_launch_count = 0;
+  int forced_width = 0;
+  if (options) {
+    for (int r : options->reserved)
+      if (r != 0)
+        return SEGTOPK_ERROR_INVALID_VALUE;
+    if (options->cluster_width < 0 || options->cluster_width > 16)
+      return SEGTOPK_ERROR_INVALID_VALUE;
+    forced_width = options->cluster_width;
+  }
+  int v = validate(key_dtype, keys, values, segment_offsets, num_segments, k, direction, determinism,
+                   tie_break, ordering, out_keys, out_values, max_segment_len);
+  if (v >= 0)
+    return v;
+  DeviceInfo dev;
+  cudaError_t e = device_info(&dev);
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  if (dev.major != 10 || dev.minor != 3)
+    return SEGTOPK_ERROR_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+
+  int64_t max_len = max_segment_len;
+  if (max_len < 0) {
+    // unknown bound: read the offsets back (synchronising)
+    std::vector<int64_t> h((size_t)num_segments + 1);
+    e = cudaMemcpyAsync(h.data(), segment_offsets, h.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+      e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+      return cuda_fail(e);
+    max_len = 0;
+    for (int64_t s = 0; s < num_segments; ++s)
+      max_len = std::max(max_len, h[(size_t)s + 1] - h[(size_t)s]);
+    if (max_len > SEGTOPK_MAX_SEGMENT_LEN)
+      return SEGTOPK_ERROR_NOT_SUPPORTED;
+  }
+  if (max_len <= 0)
+    return SEGTOPK_SUCCESS;
+
+  const KeyOps& ops = *ops_for(key_dtype);
+  Plan pl;
+  if (forced_width > 0) {
+    pl = size_plan(ops, k, forced_width);
+    int resident = 0;
+    e = ops.occupancy(pl.shape, &resident);
+    if (e != cudaSuccess || resident <= 0) {
+      (void)cudaGetLastError();
+      return SEGTOPK_ERROR_NOT_SUPPORTED;
+    }
+  } else {
+    e = choose_plan(ops, num_segments, max_len, k, &pl);
+    if (e != cudaSuccess)
+      return cuda_fail(e);
+  }
+
+  KernelParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.keys = keys;
+  p.values = values;
+  p.offsets = segment_offsets;
+  p.out_keys = out_keys;
+  p.out_values = out_values;
+  p.num_segments = num_segments;
+  p.n_lo = 0;
+  p.n_hi = max_len;
+  p.dirmask = (direction == SEGTOPK_MAX) ? ~0ull : 0ull;
+  if (ops.rank_bits == 16)
+    p.dirmask &= 0xffffull;
+  else if (ops.rank_bits == 32)
+    p.dirmask &= 0xffffffffull;
+  p.k = k;
+  p.list_cap = pl.list_cap;
+  p.ring_stages = kStages;
+  p.ring_bytes = pl.ring_bytes;
+  p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;
+  p.sorted = (ordering != SEGTOPK_UNSORTED) ? 1 : 0;
+  p.flag_overlong = 1;
+  e = ops.launch(p, pl.shape, st);
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  t_last_launch_count = 1;
+  return SEGTOPK_SUCCESS;
+}
+
+extern "C" int segtopk_batched_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+                                    const int64_t* segment_offsets, int64_t num_segments, int32_t k,
+                                    segtopk_direction direction, segtopk_determinism determinism,
+                                    segtopk_tie_break tie_break, segtopk_ordering ordering,
+                                    void* out_keys, int32_t* out_values, int64_t max_segment_len,
+                                    void* stream)
+{
+  return segtopk_batched_topk_ex(key_dtype, keys, values, segment_offsets, num_segments, k, direction,
+                                 determinism, tie_break, ordering, out_keys, out_values, max_segment_len,
+                                 nullptr, stream);
+}
+
+namespace {
+size_t ws_align(size_t x) { return (x + 255) & ~(size_t)255; }
+int key_bytes_of(int dtype)
+{
+  switch (dtype) {
+  case SEGTOPK_F16:
+  case SEGTOPK_BF16: return 2;
+  case SEGTOPK_F64: return 8;
+  default: return 4;
+  }
+}
+} // namespace
+
+extern "C" size_t segtopk_host_workspace_bytes(segtopk_dtype key_dtype, int has_values, int64_t num_keys,
+                                               int64_t num_segments, int32_t k)
+{
+  if (num_keys < 0 || num_segments < 0 || k < 0)
+    return 0;
+  const size_t kb = (size_t)key_bytes_of(key_dtype);
+  size_t b = ws_align((size_t)num_keys * kb) + ws_align((size_t)(num_segments + 1) * 8) +
+             ws_align((size_t)num_segments * (size_t)k * kb);
+  if (has_values)
+    b += ws_align((size_t)num_keys * 4) + ws_align((size_t)num_segments * (size_t)k * 4);
+  return b;
+}
+
+extern "C" int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+                                         const int64_t* segment_offsets, int64_t num_segments, int32_t k,
+                                         segtopk_direction direction, segtopk_determinism determinism,
+                                         segtopk_tie_break tie_break, segtopk_ordering ordering,
+                                         void* out_keys, int32_t* out_values, int64_t max_segment_len,
+                                         void* device_workspace, size_t workspace_bytes, void* stream)
+{
+  t_last_launch_count = 0;
+  int v = validate(key_dtype, keys ? (const void*)16 : nullptr, values, segment_offsets, num_segments, k,
+                   direction, determinism, tie_break, ordering, out_keys, out_values, max_segment_len);
+  if (v >= 0)
+    return v;
+  if (!device_workspace)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if (((uintptr_t)device_workspace & 255u) != 0)
+    return SEGTOPK_ERROR_MISALIGNED;
+  // keys addressed by the offsets: the host reads its own offsets array
+  int64_t num_keys = 0, max_len = 0;
+  for (int64_t s = 0; s < num_segments; ++s) {
+    num_keys = std::max(num_keys, segment_offsets[s + 1]);
+    max_len = std::max(max_len, segment_offsets[s + 1] - segment_offsets[s]);
+  }
+  if (max_segment_len >= 0)
+    max_len = std::min(max_len, max_segment_len);
+  if (max_len > SEGTOPK_MAX_SEGMENT_LEN)
+    return SEGTOPK_ERROR_NOT_SUPPORTED;
+  const size_t need = segtopk_host_workspace_bytes(key_dtype, values != nullptr, num_keys, num_segments, k);
+  if (workspace_bytes < need)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  const size_t kb = (size_t)key_bytes_of(key_dtype);
+  char* w = (char*)device_workspace;
+  void* d_keys = w;
+  w += ws_align((size_t)num_keys * kb);
+  int64_t* d_offs = (int64_t*)w;
+  w += ws_align((size_t)(num_segments + 1) * 8);
+  void* d_out_keys = w;
+  w += ws_align((size_t)num_segments * (size_t)k * kb);
+  int32_t* d_values = nullptr;
+  int32_t* d_out_values = nullptr;
+  if (values) {
+    d_values = (int32_t*)w;
+    w += ws_align((size_t)num_keys * 4);
+    d_out_values = (int32_t*)w;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(d_keys, keys, (size_t)num_keys * kb, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(d_offs, segment_offsets, (size_t)(num_segments + 1) * 8, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && values)
+    e = cudaMemcpyAsync(d_values, values, (size_t)num_keys * 4, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  // slots past a short segment's length keep the caller's host contents
+  e = cudaMemcpyAsync(d_out_keys, out_keys, (size_t)num_segments * (size_t)k * kb, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && values)
+    e = cudaMemcpyAsync(d_out_values, out_values, (size_t)num_segments * (size_t)k * 4, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  int rc = segtopk_batched_topk(key_dtype, d_keys, d_values, d_offs, num_segments, k, direction, determinism,
+                                tie_break, ordering, d_out_keys, d_out_values, max_len, stream);
+  if (rc != SEGTOPK_SUCCESS)
+    return rc;
+  const int launches = t_last_launch_count;
+  e = cudaMemcpyAsync(out_keys, d_out_keys, (size_t)num_segments * (size_t)k * kb, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess && values)
+    e = cudaMemcpyAsync(out_values, d_out_values, (size_t)num_segments * (size_t)k * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess)
+    e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  t_last_launch_count = launches;
+  return SEGTOPK_SUCCESS;
+}
+
+extern "C" const char* segtopk_status_string(int status)
+{
+  switch (status) {
+  case SEGTOPK_SUCCESS: return "success";
+  case SEGTOPK_ERROR_INVALID_VALUE: return "invalid argument value";
+  case SEGTOPK_ERROR_INVALID_COMBINATION: return "determinism / tie_break combination not allowed";
+  case SEGTOPK_ERROR_NOT_SUPPORTED: return "request outside the supported limits";
+  case SEGTOPK_ERROR_MISALIGNED: return "keys pointer is not 16-byte aligned";
+  case SEGTOPK_ERROR_CUDA: return "CUDA runtime error";
+  case SEGTOPK_ERROR_DEVICE: return "unsupported device (needs sm_103)";
+  default: return "unknown status";
+  }
+}
+
+extern "C" int segtopk_last_cuda_error(void) { return t_last_cuda_error; }
+
+extern "C" int segtopk_last_launch_count(void) { return t_last_launch_count; }
+
+extern "C" int segtopk_read_device_error(uint32_t* error_word)
+{
+  if (!error_word)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  uint32_t all = 0;
+  const KeyOps* list[] = {&key_ops_f16(), &key_ops_bf16(), &key_ops_f32(),
+                          &key_ops_f64(), &key_ops_u32(), &key_ops_i32()};
+  for (const KeyOps* o : list) {
+    uint32_t w = 0;
+    e = o->read_error(&w);
+    if (e != cudaSuccess)
+      return cuda_fail(e);
+    all |= w;
+  }
+  *error_word = all;
+  return SEGTOPK_SUCCESS;
+}

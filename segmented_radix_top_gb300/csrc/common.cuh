@@ -1,0 +1,265 @@
+// Shared device helpers for the segmented top-k kernels (sm_103a).
+//
+// Inline PTX for: 1-D bulk copies (TMA) driven by mbarriers, thread-block
+// cluster barriers and distributed shared memory (DSMEM) access, plus the
+// order-preserving key transform.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace segtopk {
+
+// ---------------------------------------------------------------------------
+// Device error word (read and cleared by segtopk_read_device_error).
+// ---------------------------------------------------------------------------
+enum : uint32_t {
+  kErrCopyTimeout = 1u,   // an mbarrier wait on a bulk copy gave up
+  kErrSegmentTooLong = 2u // a segment exceeded the planned length class
+};
+// One error word per translation unit (read by that unit's host accessor).
+static __device__ uint32_t g_device_error;
+
+__device__ __forceinline__ void raise_error(uint32_t bits) { atomicOr(&g_device_error, bits); }
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses, mbarriers and bulk copies
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+// Global -> shared bulk copy (TMA, 1-D). dst, src 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+  asm volatile(
+    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+      smem_addr(dst)),
+    "l"(src), "r"(bytes), "r"(smem_addr(bar))
+    : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+  uint32_t ok;
+  asm volatile(
+    "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+    : "=r"(ok)
+    : "r"(smem_addr(bar)), "r"(parity)
+    : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after about one second of SM clock cycles, records
+// the failure and lets the caller continue on a uniform control path.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+{
+  if (mbar_try_wait(bar, parity))
+    return true;
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - start > (1ll << 31)) {
+      raise_error(kErrCopyTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters and DSMEM
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank()
+{
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive()
+{
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_sync()
+{
+  cluster_arrive();
+  cluster_wait();
+}
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local_smem_addr, uint32_t rank)
+{
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v)
+{
+  asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr)
+{
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint16_t v)
+{
+  asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v)
+{
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint64_t v)
+{
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Order-preserving key transform.
+//
+// T maps a key's bits to an unsigned integer whose order is the key's numeric
+// order: floats flip the sign bit of non-negative values and invert all bits
+// of negative ones; -0.0 is first replaced by +0.0 so that both zeros get one
+// code ("Fix BlockTopK +/-0.0 handling", Cause: canonicalise the zero before
+// any direction handling, never compare raw bits against extracted digits).
+// Signed integers flip the sign bit; unsigned integers are unchanged.
+//
+// The selection works on the rank code r = T(x) XOR dirmask, where dirmask is
+// all ones for "max" and zero for "min", so that a smaller r is always a
+// better key. XOR-ing every bit reverses every radix digit, i.e. the bucket
+// index b becomes num_buckets-1-b for the max direction -- the bucket
+// reversal of the same page's Fix section -- and the raw key bits are only
+// ever copied, never compared.
+// ---------------------------------------------------------------------------
+enum class KeyKind : int { F16 = 0, BF16 = 1, F32 = 2, F64 = 3, U32 = 4, I32 = 5 };
+
+template <KeyKind K>
+struct KeyTraits;
+
+template <>
+struct KeyTraits<KeyKind::F16> {
+  using Raw = uint16_t;
+  using Rank = uint32_t;
+  static constexpr int kRankBits = 16;
+  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask)
+  {
+    uint32_t v = (x == 0x8000u) ? 0u : x;
+    uint32_t neg = 0u - (v >> 15);
+    return ((v ^ (neg | 0x8000u)) & 0xffffu) ^ dirmask;
+  }
+};
+template <>
+struct KeyTraits<KeyKind::BF16> : KeyTraits<KeyKind::F16> {};
+
+template <>
+struct KeyTraits<KeyKind::F32> {
+  using Raw = uint32_t;
+  using Rank = uint32_t;
+  static constexpr int kRankBits = 32;
+  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask)
+  {
+    uint32_t v = (x == 0x80000000u) ? 0u : x;
+    uint32_t neg = 0u - (v >> 31);
+    return (v ^ (neg | 0x80000000u)) ^ dirmask;
+  }
+};
+
+template <>
+struct KeyTraits<KeyKind::F64> {
+  using Raw = uint64_t;
+  using Rank = uint64_t;
+  static constexpr int kRankBits = 64;
+  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask)
+  {
+    uint64_t v = (x == 0x8000000000000000ull) ? 0ull : x;
+    uint64_t neg = 0ull - (v >> 63);
+    return (v ^ (neg | 0x8000000000000000ull)) ^ dirmask;
+  }
+};
+
+template <>
+struct KeyTraits<KeyKind::U32> {
+  using Raw = uint32_t;
+  using Rank = uint32_t;
+  static constexpr int kRankBits = 32;
+  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return x ^ dirmask; }
+};
+
+template <>
+struct KeyTraits<KeyKind::I32> {
+  using Raw = uint32_t;
+  using Rank = uint32_t;
+  static constexpr int kRankBits = 32;
+  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return (x ^ 0x80000000u) ^ dirmask; }
+};
+
+// ---------------------------------------------------------------------------
+// Warp helpers
+// ---------------------------------------------------------------------------
+constexpr uint32_t kFull = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+  uint32_t m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ uint32_t warp_inclusive_sum(uint32_t x)
+{
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_up_sync(kFull, x, o);
+    if (lane >= (uint32_t)o)
+      x += y;
+  }
+  return x;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_max(T x)
+{
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    T y = __shfl_xor_sync(kFull, x, o);
+    x = y > x ? y : x;
+  }
+  return x;
+}
+
+} // namespace segtopk

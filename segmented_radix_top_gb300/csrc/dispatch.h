@@ -1,0 +1,37 @@
+// Host-side interface between the C ABI (api.cu) and the per-key-type kernel
+// translation units (inst_*.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace segtopk {
+
+struct KernelParams;
+
+struct LaunchShape {
+  int threads;        // CTA size
+  int cluster;        // CTAs per segment (1 = plain launch)
+  uint32_t smem;      // dynamic shared memory bytes
+};
+
+// Entry points every key-type translation unit provides.
+struct KeyOps {
+  int key_bytes;
+  int rank_bits;
+  // Launch the segment kernel over all num_segments segments.
+  cudaError_t (*launch)(const KernelParams& p, const LaunchShape& s, cudaStream_t stream);
+  // Resident clusters (cluster > 1) or resident CTAs (cluster == 1) per GPU.
+  cudaError_t (*occupancy)(const LaunchShape& s, int* resident);
+  // Read and clear this translation unit's device error word (synchronous).
+  cudaError_t (*read_error)(uint32_t* word);
+};
+
+const KeyOps& key_ops_f16();
+const KeyOps& key_ops_bf16();
+const KeyOps& key_ops_f32();
+const KeyOps& key_ops_f64();
+const KeyOps& key_ops_u32();
+const KeyOps& key_ops_i32();
+
+} // namespace segtopk

@@ -1,0 +1,106 @@
+// Launch helpers shared by the per-key-type translation units.
+#pragma once
+
+#include "dispatch.h"
+#include "stream_topk.cuh"
+
+namespace segtopk {
+
+template <KeyKind KK, int NT>
+struct StreamLauncher {
+  static cudaError_t prepare(uint32_t smem, int cluster)
+  {
+    // Raise the dynamic shared-memory opt-in lazily, only as far as needed.
+    static uint32_t granted = 0;
+    static bool nonportable = false;
+    auto fn = stream_topk_kernel<KK, NT>;
+    if (smem > granted) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess)
+        return e;
+      granted = smem;
+    }
+    if (cluster > 8 && !nonportable) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess)
+        return e;
+      nonportable = true;
+    }
+    return cudaSuccess;
+  }
+
+  static void config(const LaunchShape& s, int64_t num_segments, cudaLaunchConfig_t& cfg,
+                     cudaLaunchAttribute* attr)
+  {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = dim3((unsigned)(num_segments * s.cluster), 1, 1);
+    cfg.blockDim = dim3(NT, 1, 1);
+    cfg.dynamicSmemBytes = s.smem;
+    cfg.numAttrs = 0;
+    cfg.attrs = attr;
+    if (s.cluster > 1) {
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)s.cluster;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.numAttrs = 1;
+    }
+  }
+
+  static cudaError_t launch(const KernelParams& p, const LaunchShape& s, cudaStream_t stream)
+  {
+    cudaError_t e = prepare(s.smem, s.cluster);
+    if (e != cudaSuccess)
+      return e;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    config(s, p.num_segments, cfg, attr);
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, stream_topk_kernel<KK, NT>, p);
+  }
+
+  static cudaError_t occupancy(const LaunchShape& s, int* resident)
+  {
+    cudaError_t e = prepare(s.smem, s.cluster);
+    if (e != cudaSuccess)
+      return e;
+    if (s.cluster <= 1) {
+      int per_sm = 0, dev = 0, sms = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_topk_kernel<KK, NT>, NT, s.smem);
+      if (e != cudaSuccess)
+        return e;
+      e = cudaGetDevice(&dev);
+      if (e != cudaSuccess)
+        return e;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      *resident = per_sm * sms;
+      return e;
+    }
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    config(s, s.cluster, cfg, attr);
+    return cudaOccupancyMaxActiveClusters(resident, stream_topk_kernel<KK, NT>, &cfg);
+  }
+};
+
+inline cudaError_t read_and_clear(uint32_t* word)
+{
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(word, g_device_error, sizeof(uint32_t));
+  if (e != cudaSuccess)
+    return e;
+  return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t));
+}
+
+} // namespace segtopk
+
+#define SEGTOPK_DEFINE_KEY_OPS(NAME, KIND)                                                         \
+  namespace segtopk {                                                                              \
+  const KeyOps& key_ops_##NAME()                                                                   \
+  {                                                                                                \
+    static const KeyOps ops = {(int)sizeof(KeyTraits<KIND>::Raw), KeyTraits<KIND>::kRankBits,     \
+                               &StreamLauncher<KIND, 256>::launch,                                 \
+                               &StreamLauncher<KIND, 256>::occupancy, &read_and_clear};            \
+    return ops;                                                                                    \
+  }                                                                                                \
+  }

@@ -1,0 +1,135 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle,
+bit-exact, on seeded inputs that span several 16 KiB chunks, ragged tails,
+unaligned segment starts, single CTAs and forced thread-block clusters."""
+import itertools
+
+import numpy as np
+import pytest
+
+from segmented_radix_top_gb300 import workloads as W
+from tests.gpu_util import check_workload, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = ["f16", "bf16", "f32", "f64", "u32", "i32"]
+TIES = ["unspecified", "prefer_smaller_index", "prefer_larger_index"]
+ORDERINGS = ["unsorted", "sorted", "stable_sorted"]
+# ragged lengths: empty, tiny, around vector / chunk boundaries, several chunks
+LENGTHS = [0, 1, 2, 3, 5, 7, 8, 9, 15, 16, 17, 31, 100, 1000, 2047, 2048, 2049, 4095, 4096, 4097,
+           8191, 8193, 12000, 20000, 40001]
+
+
+def det_for(tie, i):
+    if tie != "unspecified":
+        return "gpu_to_gpu"
+    return ["not_guaranteed", "run_to_run", "gpu_to_gpu"][i % 3]
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("direction", ["max", "min"])
+@pytest.mark.parametrize("tie", TIES)
+def test_single_cta_matrix(dtype, direction, tie):
+    for i, (k, distinct) in enumerate([(1, None), (7, 5), (50, None), (300, 40), (2048, None)]):
+        ordering = ORDERINGS[i % 3]
+        wl = W.random_workload(100 + i, dtype, LENGTHS, k, direction, det_for(tie, i), tie, ordering,
+                               pairs=(i % 2 == 0), distinct=distinct, lead=1 + i)
+        check_workload(wl, cluster_width=1, where="%s/%s/%s k=%d %s" % (dtype, direction, tie, k, ordering))
+
+
+@pytest.mark.parametrize("width", [2, 3, 4, 8, 16])
+@pytest.mark.parametrize("dtype", ["f16", "f32", "f64", "u32"])
+def test_cluster_widths(width, dtype):
+    lengths = [0, 1, 3, width - 1, width, 17, 100, 4097, 30000, 70001, 131072]
+    for i, (k, tie, ordering, distinct) in enumerate([
+            (5, "prefer_smaller_index", "stable_sorted", None),
+            (64, "prefer_larger_index", "unsorted", 7),
+            (1024, "prefer_smaller_index", "sorted", 300),
+            (33, "prefer_larger_index", "stable_sorted", 3)]):
+        direction = "max" if i % 2 == 0 else "min"
+        wl = W.random_workload(500 + i, dtype, lengths, k, direction, "gpu_to_gpu", tie, ordering,
+                               pairs=True, distinct=distinct, lead=3)
+        check_workload(wl, cluster_width=width, where="C=%d %s k=%d %s %s" % (width, dtype, k, tie, ordering))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "f64"])
+def test_signed_zero_and_infinities(dtype):
+    """Only +/-0.0, +/-inf and a few numbers: zeros tie and keep their bits."""
+    g = np.random.Generator(np.random.PCG64(9))
+    n = 30000
+    x = g.choice(np.array([0.0, -0.0, np.inf, -np.inf, 1.0, -1.0]), size=n, p=[.3, .3, .05, .05, .15, .15])
+    bits = {"f16": W.f16_bits, "f32": W.f32_bits, "f64": W.f64_bits}[dtype](x)
+    lengths = [17, 1000, 9000, 19983]
+    offs = W.offsets_from_lengths(lengths)
+    for direction, tie, k in itertools.product(["max", "min"], TIES[1:], [3, 700, 2048]):
+        wl = W.Workload("zeros", dtype, bits[: offs[-1]], np.arange(offs[-1], dtype=np.int32), offs, k,
+                        direction, "gpu_to_gpu", tie, "stable_sorted")
+        for width in (1, 2):
+            check_workload(wl, cluster_width=width, where="zeros %s %s %s k=%d C=%d" % (
+                dtype, direction, tie, k, width))
+
+
+def test_nan_order_reading():
+    """NaNs (pages silent): +NaN above +inf and -NaN below -inf, payload order."""
+    bits = np.array([0x7F800000, 0x7FC00001, 0xFF800000, 0xFFC00100, 0x7FC00100, 0xFFC00001, 0,
+                     0x3F800000] * 700, dtype=np.uint32)
+    offs = np.array([0, 5, 5600], dtype=np.int64)
+    for direction in ("max", "min"):
+        wl = W.Workload("nan", "f32", bits, np.arange(len(bits), dtype=np.int32), offs, 9, direction,
+                        "gpu_to_gpu", "prefer_smaller_index", "stable_sorted")
+        check_workload(wl, cluster_width=1)
+        check_workload(wl, cluster_width=2)
+
+
+@pytest.mark.parametrize("pattern", ["ascending", "descending", "all_equal", "two_values", "sawtooth"])
+@pytest.mark.parametrize("tie", ["prefer_smaller_index", "prefer_larger_index"])
+def test_adversarial_orders(pattern, tie):
+    """Orders that make the candidate list refill and trim repeatedly."""
+    n = 200000
+    i = np.arange(n, dtype=np.int64)
+    if pattern == "ascending":
+        x = i.astype(np.uint32)
+    elif pattern == "descending":
+        x = (n - i).astype(np.uint32)
+    elif pattern == "all_equal":
+        x = np.full(n, 77, dtype=np.uint32)
+    elif pattern == "two_values":
+        x = np.where(i % 3 == 0, 5, 9).astype(np.uint32)
+    else:
+        x = (i % 5000).astype(np.uint32)
+    lengths = [n // 2, n // 4, n // 4]
+    for direction, k in itertools.product(["max", "min"], [1, 100, 1500]):
+        wl = W.Workload(pattern, "u32", x, i.astype(np.int32), W.offsets_from_lengths(lengths), k,
+                        direction, "gpu_to_gpu", tie, "stable_sorted")
+        for width in (1, 4):
+            check_workload(wl, cluster_width=width, where="%s %s %s k=%d C=%d" % (
+                pattern, tie, direction, k, width))
+
+
+def test_offsets_edge_cases():
+    """Decreasing offsets (empty), a zero-length batch of segments, n == k,
+    n == k + 1, every segment shorter than k."""
+    g = np.random.Generator(np.random.PCG64(3))
+    keys = W.random_keys(g, "f32", 5000)
+    vals = np.arange(5000, dtype=np.int32)
+    offs = np.array([0, 10, 4, 4, 20, 60, 61, 61, 4000, 3000, 5000], dtype=np.int64)
+    for k in (1, 10, 40, 41, 2048):
+        for order in ORDERINGS:
+            wl = W.Workload("edges", "f32", keys, vals, offs, k, "max", "gpu_to_gpu",
+                            "prefer_smaller_index", order)
+            check_workload(wl, cluster_width=1, where="edges k=%d %s" % (k, order))
+            check_workload(wl, cluster_width=3, where="edges k=%d %s C=3" % (k, order))
+
+
+def test_unknown_max_segment_len():
+    wl = W.random_workload(4, "f32", [10, 5000, 300], 20, pairs=True, lead=5)
+    check_workload(wl, max_segment_len=None)
+
+
+def test_repeat_runs_identical():
+    """Deterministic modes give bit-identical outputs run after run, in every
+    ordering (this implementation's unsorted order is fixed too)."""
+    wl = W.workload3(segments=300)
+    a = run_gpu(wl)
+    for _ in range(3):
+        b = run_gpu(wl)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
