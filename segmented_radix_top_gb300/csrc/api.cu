@@ -2,7 +2,9 @@
 // and dispatch to the per-key-type kernels. See include/segtopk.h.
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "../../include/segtopk.h"
@@ -130,6 +132,53 @@ cudaError_t choose_plan(const KeyOps& ops, int64_t num_segments, int64_t max_len
   return have ? cudaSuccess : cudaErrorInvalidConfiguration;
 }
 
+// Plans are cached per (device, key type, num_segments, max_len, k, forced
+// width): after the first call a call only validates and launches, so it can
+// also be captured into a CUDA graph.
+using PlanKey = std::tuple<int, int, int64_t, int64_t, int32_t, int>;
+std::mutex g_plan_mu;
+std::map<PlanKey, Plan> g_plans;
+
+cudaError_t get_plan(int dtype, const KeyOps& ops, int64_t num_segments, int64_t max_len, int32_t k,
+                     int forced_width, Plan* out, bool* unsupported)
+{
+  *unsupported = false;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess)
+    return e;
+  const PlanKey key(dev, dtype, num_segments, max_len, k, forced_width);
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    auto it = g_plans.find(key);
+    if (it != g_plans.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  Plan pl;
+  if (forced_width > 0) {
+    pl = size_plan(ops, k, forced_width);
+    int resident = 0;
+    e = ops.occupancy(pl.shape, &resident);
+    if (e != cudaSuccess || resident <= 0) {
+      (void)cudaGetLastError();
+      *unsupported = true;
+      return cudaSuccess;
+    }
+  } else {
+    e = choose_plan(ops, num_segments, max_len, k, &pl);
+    if (e != cudaSuccess)
+      return e;
+  }
+  std::lock_guard<std::mutex> lk(g_plan_mu);
+  if (g_plans.size() > 4096)
+    g_plans.clear();
+  g_plans[key] = pl;
+  *out = pl;
+  return cudaSuccess;
+}
+
 bool valid_pair(int det, int tie)
 {
   if (tie == SEGTOPK_TIE_UNSPECIFIED)
@@ -224,19 +273,12 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
 
   const KeyOps& ops = *ops_for(key_dtype);
   Plan pl;
-  if (forced_width > 0) {
-    pl = size_plan(ops, k, forced_width);
-    int resident = 0;
-    e = ops.occupancy(pl.shape, &resident);
-    if (e != cudaSuccess || resident <= 0) {
-      (void)cudaGetLastError();
-      return SEGTOPK_ERROR_NOT_SUPPORTED;
-    }
-  } else {
-    e = choose_plan(ops, num_segments, max_len, k, &pl);
-    if (e != cudaSuccess)
-      return cuda_fail(e);
-  }
+  bool unsupported = false;
+  e = get_plan(key_dtype, ops, num_segments, max_len, k, forced_width, &pl, &unsupported);
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  if (unsupported)
+    return SEGTOPK_ERROR_NOT_SUPPORTED;
 
   KernelParams p;
   std::memset(&p, 0, sizeof(p));
