@@ -57,7 +57,9 @@ typedef enum {
 } segtopk_tie_break;
 
 /* Output order of the selected items (same page, "Output ordering" table).
- * UNSORTED: any order (this library writes a fixed, repeatable order).
+ * UNSORTED: any order; with a deterministic mode the set is fixed but the
+ *         positions may differ from run to run (set membership, not
+ *         positions, is what determinism pins).
  * SORTED: by key, better first; equal keys in unspecified order (this
  *         library writes them in source-index order, i.e. as STABLE_SORTED).
  * STABLE_SORTED: by key, better first; equal keys by source index ascending,

@@ -75,27 +75,41 @@ constexpr int kThreads = 256;
 struct Plan {
   LaunchShape shape;
   uint32_t list_cap;
+  uint32_t trim_at;
   uint32_t ring_bytes;
+  bool merge_gather;
 };
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Shared-memory sizing for a given k and cluster width.
+// Candidate-list slack: entries appended after a trim before the next one.
+constexpr uint32_t kListSlack = 512;
+
+// Shared-memory sizing for a given k and cluster width. The list must absorb
+// a whole chunk after reaching the trim threshold; the ring doubles as sort
+// scratch and, in a cluster leader, as gather space.
 Plan size_plan(const KeyOps& ops, int32_t k, int cluster)
 {
   Plan pl;
   const uint32_t kb = (uint32_t)ops.key_bytes;
   const uint32_t chunk_keys = kChunkBytes / kb;
-  pl.list_cap = align_up((uint32_t)k + chunk_keys, 32);
-  // the ring doubles as sort scratch (and, in a cluster leader, as gather space)
-  uint32_t sort_need = sort_scratch_bytes((uint32_t)k, ops.rank_bits);
-  if (cluster > 1)
-    sort_need += align_up((uint32_t)k * kb, 16) + align_up((uint32_t)k * 4u, 16);
-  pl.ring_bytes = align_up(std::max(kStages * kChunkBytes, sort_need), 128);
-  uint32_t smem = kCtrlBytes + pl.ring_bytes + align_up(pl.list_cap * kb, 16) + pl.list_cap * 4u;
+  const uint32_t uk = (uint32_t)k;
+  pl.list_cap = align_up(uk + chunk_keys + kListSlack, 32);
+  pl.trim_at = pl.list_cap - chunk_keys;
+  const uint32_t stream_ring = kStages * kChunkBytes;
+  const uint32_t sort_need = sort_scratch_bytes(uk, ops.rank_bits);
+  uint32_t need = sort_need;
+  pl.merge_gather = false;
+  if (cluster > 1) {
+    const uint32_t cap = (uint32_t)cluster * uk;
+    const uint32_t gather_need = align16(cap * kb) + align16(cap * 4u) + sort_need;
+    pl.merge_gather = gather_need <= stream_ring;
+    need = pl.merge_gather ? gather_need : align16(uk * kb) + align16(uk * 4u) + sort_need;
+  }
+  pl.ring_bytes = align_up(std::max(stream_ring, need), 128);
   pl.shape.threads = kThreads;
   pl.shape.cluster = cluster;
-  pl.shape.smem = smem;
+  pl.shape.smem = kCtrlBytes + pl.ring_bytes + list_bytes(pl.list_cap, kb);
   return pl;
 }
 
@@ -297,6 +311,8 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
     p.dirmask &= 0xffffffffull;
   p.k = k;
   p.list_cap = pl.list_cap;
+  p.trim_at = pl.trim_at;
+  p.merge_gather = pl.merge_gather ? 1 : 0;
   p.ring_stages = kStages;
   p.ring_bytes = pl.ring_bytes;
   p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;

@@ -1,14 +1,13 @@
 // Block-level building blocks of the per-segment selection:
-//   * radix digit selection over a candidate list held in shared memory,
-//   * index-ordered compaction of the selected entries (warp ballots + a
-//     block prefix scan), and
+//   * radix digit selection (most significant digit first, with early stop)
+//     over a candidate list held in shared memory,
+//   * the composite selection that resolves boundary ties by source index,
+//   * compaction of the selected entries at positions from warp ballots and a
+//     block prefix scan, and
 //   * a bitonic sort of the selected items for sorted output.
 //
 // The list is a structure of arrays in shared memory: raw key bits and the
-// segment-local source index of every entry. Entries are kept in preference
-// order: ascending source index for prefer_smaller_index (and unspecified),
-// descending for prefer_larger_index. Among equal keys an earlier entry is
-// therefore always the preferred one.
+// segment-local source index of every entry, in no particular order.
 #pragma once
 
 #include "common.cuh"
@@ -21,33 +20,21 @@ constexpr int kBuckets = 1 << kDigitBits;
 // Control block at the start of dynamic shared memory. Every CTA of a cluster
 // has the same layout, so a field can be addressed in a peer through DSMEM.
 struct Ctrl {
-  uint64_t bars[8];            // one mbarrier per ring stage
-  uint64_t scan_tot[2][32];    // per-warp packed totals of the block scans (double buffered)
-  uint32_t hist[2][kBuckets];  // digit histograms (double buffered; zero outside a selection)
+  uint64_t bars[8];               // one mbarrier per ring stage
+  uint64_t scan_tot[2][32];       // per-warp packed totals of the block scans (double buffered)
+  uint64_t red[32];               // block reductions
+  uint32_t hist[2][kBuckets];     // digit histograms (double buffered; zero outside a selection)
   uint32_t hist_merged[kBuckets]; // cluster leader: histogram pushed by the other CTAs
-  uint32_t res[4];             // selection result of a pass: bucket, count before, bucket count
-  uint32_t front_base;         // cross-CTA scan: selected entries of preceding CTAs
-  uint32_t tie_base;           // cross-CTA scan: boundary ties of preceding CTAs
-  uint32_t counts[2];          // this CTA's (front, tie) totals
-  uint64_t red[32];            // block reductions
+  uint32_t res[4];                // selection result of a pass: bucket, count before, bucket count
+  uint32_t list_count;            // entries in the candidate list
+  uint32_t gather_count;          // cluster leader: entries gathered from the cluster
+  uint32_t front_base;            // cross-CTA scan: selected entries of preceding CTAs
+  uint32_t tie_base;              // cross-CTA scan: boundary ties of preceding CTAs
 };
 constexpr uint32_t kCtrlBytes = (sizeof(Ctrl) + 127u) & ~127u;
 
-// Result of a radix selection: the k best entries are those with
-// (rank & mask) < prefix ("front", strictly better than every boundary
-// candidate) plus the first `ties` entries (in list order) with
-// (rank & mask) == prefix. `mask` covers the resolved leading digits; it is
-// all ones unless the selection stopped early because the boundary bucket
-// held exactly the remaining count.
-template <typename Rank>
-struct Selection {
-  Rank prefix;
-  Rank mask;
-  uint32_t ties;
-};
-
 // Warp 0 of the block: find the bucket holding the krem-th best candidate.
-// `h` gives the 8 bucket counts this lane owns (buckets 8*lane .. 8*lane+7).
+// `h` holds the 8 bucket counts this lane owns (buckets 8*lane .. 8*lane+7).
 // Writes bucket, count before it and its count to res[].
 __device__ __forceinline__ void find_bucket(const uint32_t (&h)[8], uint32_t krem, uint32_t* res)
 {
@@ -77,84 +64,137 @@ __device__ __forceinline__ void find_bucket(const uint32_t (&h)[8], uint32_t kre
   }
 }
 
-// Histogram of one digit over the list entries whose resolved digits match.
-template <class TR, int NT>
-__device__ __forceinline__ void build_hist(const typename TR::Raw* raw, uint32_t count,
-                                           typename TR::Rank dirmask, typename TR::Rank prefix,
-                                           typename TR::Rank mask, int shift, uint32_t* h)
-{
-  using Rank = typename TR::Rank;
-  for (uint32_t e = threadIdx.x; e < count; e += NT) {
-    const Rank r = TR::rank(raw[e], dirmask);
-    if ((r & mask) == prefix)
-      atomicAdd(&h[(uint32_t)(r >> shift) & (kBuckets - 1)], 1u);
-  }
-}
+template <class Key>
+struct Radix {
+  Key prefix;      // resolved leading digits of the boundary key
+  Key mask;        // which digits are resolved
+  uint32_t krem;   // how many boundary candidates are still needed
+  bool stopped;    // the boundary bucket held exactly krem candidates
+};
 
-// Radix selection of the kk best of the first `count` list entries
-// (count > kk > 0) inside one CTA: most-significant digit first, each pass
-// histograms the digit over the candidates, finds the bucket holding the
-// kk-th entry, narrows kk to that bucket and folds the digit into the
-// prefix; it stops early when that bucket holds exactly the remaining count
-// ("Implement Segmented TopK using Thread-Block-Clusters", sections 1.2
-// "Radix (digit) top-k" and 1.4 "Early stop").
-template <class TR, int NT>
-__device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, const typename TR::Raw* raw,
-                                                     uint32_t count, uint32_t kk,
-                                                     typename TR::Rank dirmask)
+// One radix selection over list entries [0, count): among the candidates
+// (get(e, key) returns true), find the kk best by key (smaller = better).
+// Each pass histograms one 8-bit digit of the candidates whose resolved
+// digits match, finds the bucket holding the krem-th best, narrows krem and
+// folds the digit into the prefix; it stops when that bucket holds exactly
+// krem candidates ("Implement Segmented TopK using Thread-Block-Clusters",
+// sections 1.2 "Radix (digit) top-k" and 1.4 "Early stop").
+// Requires count >= kk > 0 candidates. Block-wide; leaves both histograms zero.
+template <class Key, int KEY_BITS, int NT, class Get>
+__device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, uint32_t kk, Get&& get)
 {
-  using Rank = typename TR::Rank;
-  constexpr int RB = TR::kRankBits;
-  constexpr int P = RB / kDigitBits;
-  Rank prefix = 0, mask = 0;
-  uint32_t krem = kk;
+  constexpr int P = KEY_BITS / kDigitBits;
+  Radix<Key> r{(Key)0, (Key)0, kk, false};
   int p = 0;
   for (; p < P; ++p) {
-    const int shift = RB - kDigitBits * (p + 1);
-    build_hist<TR, NT>(raw, count, dirmask, prefix, mask, shift, ctl.hist[p & 1]);
+    const int shift = KEY_BITS - kDigitBits * (p + 1);
+    uint32_t* h = ctl.hist[p & 1];
+    for (uint32_t e = threadIdx.x; e < count; e += NT) {
+      Key key;
+      if (get(e, key) && (key & r.mask) == r.prefix)
+        atomicAdd(&h[(uint32_t)(key >> shift) & (kBuckets - 1)], 1u);
+    }
     if (threadIdx.x < kBuckets)
       ctl.hist[(p + 1) & 1][threadIdx.x] = 0;
     __syncthreads();
     if (threadIdx.x < 32) {
-      uint32_t h[8];
+      uint32_t hh[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        h[i] = ctl.hist[p & 1][8 * threadIdx.x + i];
-      find_bucket(h, krem, ctl.res);
+        hh[i] = h[8 * threadIdx.x + i];
+      find_bucket(hh, r.krem, ctl.res);
     }
     __syncthreads();
     const uint32_t b = ctl.res[0], before = ctl.res[1], cnt = ctl.res[2];
-    krem -= before;
-    prefix |= (Rank)b << shift;
-    mask |= (Rank)(kBuckets - 1) << shift;
-    if (cnt == krem)
+    r.krem -= before;
+    r.prefix |= (Key)b << shift;
+    r.mask |= (Key)(kBuckets - 1) << shift;
+    if (cnt == r.krem) {
+      r.stopped = true;
       break;
+    }
   }
   if (p == P)
     p = P - 1;
   // restore the "both histograms zero" invariant (warp 0 read this one before the last barrier)
   if (threadIdx.x < kBuckets)
     ctl.hist[p & 1][threadIdx.x] = 0;
-  Selection<Rank> s;
-  s.prefix = prefix;
-  s.mask = mask;
-  s.ties = krem;
+  __syncthreads(); // ctl.res may be rewritten by the next selection
+  return r;
+}
+
+// Preference index: smaller is preferred among equal keys.
+__device__ __forceinline__ uint32_t pref_index(uint32_t idx, bool prefer_larger)
+{
+  return prefer_larger ? ~idx : idx;
+}
+
+// Which list entries form the k best: (rank & mask) < prefix are strictly
+// better than the boundary ("front"); among the boundary candidates
+// ((rank & mask) == prefix) those with (pref_index & imask) <= iprefix are
+// taken. imask == 0 takes every boundary candidate.
+template <class Rank>
+struct Selection {
+  Rank prefix, mask;
+  uint32_t iprefix, imask;
+  // 0: not selected, 1: front, 2: selected boundary entry
+  __device__ __forceinline__ int classify(Rank r, uint32_t pidx) const
+  {
+    const Rank mr = r & mask;
+    if (mr < prefix)
+      return 1;
+    return (mr == prefix && (pidx & imask) <= iprefix) ? 2 : 0;
+  }
+};
+
+// Boundary ties by source index: among entries with (rank & mask) == prefix,
+// choose the q preferred ones (0 < q < their count) by a second radix
+// selection on the preference index, which is unique within a segment.
+template <class TR, int NT>
+__device__ void select_ties(Ctrl& ctl, const typename TR::Raw* raw, const uint32_t* idx, uint32_t count,
+                            uint32_t q, typename TR::Rank dirmask, bool prefer_larger,
+                            Selection<typename TR::Rank>& s)
+{
+  using Rank = typename TR::Rank;
+  const Rank prefix = s.prefix, mask = s.mask;
+  const Radix<uint32_t> ri = radix_select<uint32_t, 32, NT>(ctl, count, q, [&](uint32_t e, uint32_t& key) {
+    key = pref_index(idx[e], prefer_larger);
+    return (TR::rank(raw[e], dirmask) & mask) == prefix;
+  });
+  s.iprefix = ri.prefix;
+  s.imask = ri.mask;
+}
+
+// The kk best of `count` list entries (count > kk > 0) in one CTA: a radix
+// selection on the rank code, then, if more boundary entries tie than are
+// needed, one on the preference index.
+template <class TR, int NT>
+__device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, const typename TR::Raw* raw,
+                                                     const uint32_t* idx, uint32_t count, uint32_t kk,
+                                                     typename TR::Rank dirmask, bool prefer_larger)
+{
+  using Rank = typename TR::Rank;
+  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, count, kk, [&](uint32_t e, Rank& key) {
+    key = TR::rank(raw[e], dirmask);
+    return true;
+  });
+  Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u};
+  if (!rr.stopped) // every rank digit resolved and more than krem entries share the boundary rank
+    select_ties<TR, NT>(ctl, raw, idx, count, rr.krem, dirmask, prefer_larger, s);
   return s;
 }
 
-// Walks the first `count` list entries in list order and classifies each as
-// front ((rank & mask) < prefix), tie ((rank & mask) == prefix) or neither.
-// For every front or tie entry it calls
-//   sink(e, raw, idx, rank, is_front, front_rank, tie_rank)
-// where front_rank / tie_rank count the front / tie entries before e in list
-// order (warp ballots inside a warp's contiguous run of 128 entries, a block
-// scan across warps). Returns the (front, tie) totals in every thread.
-// The sink runs after a barrier that follows every thread's reads of the
-// current tile, so it may overwrite list slots at or before the tile.
-template <class TR, int NT, class Sink>
-__device__ uint2 scan_list(Ctrl& ctl, const typename TR::Raw* raw, const uint32_t* idx,
-                           uint32_t count, typename TR::Rank dirmask, typename TR::Rank prefix,
-                           typename TR::Rank mask, Sink&& sink)
+// Walks list entries [0, count); classify(e, raw, idx, rank) returns 0 (skip),
+// 1 or 2. For every entry of class 1 or 2 it calls
+//   sink(e, raw, idx, rank, cls, rank1, rank2)
+// where rank1 / rank2 count the class-1 / class-2 entries before e (warp
+// ballots over a warp's contiguous run of 128 entries, a block scan across
+// warps). Returns the class totals. The sink runs after a barrier that
+// follows every thread's reads of the current tile, so it may overwrite list
+// slots at or before the tile.
+template <class TR, int NT, class Classify, class Sink>
+__device__ uint2 scan_list(Ctrl& ctl, const typename TR::Raw* raw, const uint32_t* idx, uint32_t count,
+                           typename TR::Rank dirmask, Classify&& classify, Sink&& sink)
 {
   using Raw = typename TR::Raw;
   using Rank = typename TR::Rank;
@@ -162,14 +202,14 @@ __device__ uint2 scan_list(Ctrl& ctl, const typename TR::Raw* raw, const uint32_
   constexpr int R = 4; // rounds of 32 entries per warp and tile
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t lt = lanemask_lt();
-  uint32_t fronts_seen = 0, ties_seen = 0;
+  uint32_t seen1 = 0, seen2 = 0;
   int buf = 0;
   for (uint32_t tile = 0; tile < count; tile += NT * R) {
     Raw kr[R];
     uint32_t ki[R];
     Rank rk[R];
-    uint32_t bf[R], bt[R];
-    uint32_t wf = 0, wt = 0;
+    uint32_t b1[R], b2[R];
+    uint32_t w1 = 0, w2 = 0;
 #pragma unroll
     for (int q = 0; q < R; ++q) {
       const uint32_t e = tile + warp * (32 * R) + q * 32 + lane;
@@ -177,42 +217,42 @@ __device__ uint2 scan_list(Ctrl& ctl, const typename TR::Raw* raw, const uint32_
       kr[q] = valid ? raw[e] : Raw(0);
       ki[q] = valid ? idx[e] : 0u;
       rk[q] = TR::rank(kr[q], dirmask);
-      const Rank mr = rk[q] & mask;
-      bf[q] = __ballot_sync(kFull, valid && mr < prefix);
-      bt[q] = __ballot_sync(kFull, valid && mr == prefix);
-      wf += __popc(bf[q]);
-      wt += __popc(bt[q]);
+      const int c = valid ? classify(e, kr[q], ki[q], rk[q]) : 0;
+      b1[q] = __ballot_sync(kFull, c == 1);
+      b2[q] = __ballot_sync(kFull, c == 2);
+      w1 += __popc(b1[q]);
+      w2 += __popc(b2[q]);
     }
     if (lane == 0)
-      ctl.scan_tot[buf][warp] = (uint64_t)wf | ((uint64_t)wt << 32);
+      ctl.scan_tot[buf][warp] = (uint64_t)w1 | ((uint64_t)w2 << 32);
     __syncthreads();
-    uint32_t fb = fronts_seen, tb = ties_seen, tf = 0, tt = 0;
+    uint32_t f1 = seen1, f2 = seen2, t1 = 0, t2 = 0;
 #pragma unroll
     for (int w = 0; w < NW; ++w) {
       const uint64_t v = ctl.scan_tot[buf][w];
       if (w < (int)warp) {
-        fb += (uint32_t)v;
-        tb += (uint32_t)(v >> 32);
+        f1 += (uint32_t)v;
+        f2 += (uint32_t)(v >> 32);
       }
-      tf += (uint32_t)v;
-      tt += (uint32_t)(v >> 32);
+      t1 += (uint32_t)v;
+      t2 += (uint32_t)(v >> 32);
     }
 #pragma unroll
     for (int q = 0; q < R; ++q) {
-      const uint32_t fr = fb + __popc(bf[q] & lt);
-      const uint32_t tr = tb + __popc(bt[q] & lt);
-      const bool isf = (bf[q] >> lane) & 1u;
-      const bool ist = (bt[q] >> lane) & 1u;
-      if (isf || ist)
-        sink(tile + warp * (32 * R) + q * 32 + lane, kr[q], ki[q], rk[q], isf, fr, tr);
-      fb += __popc(bf[q]);
-      tb += __popc(bt[q]);
+      const bool is1 = (b1[q] >> lane) & 1u;
+      const bool is2 = (b2[q] >> lane) & 1u;
+      if (is1 || is2)
+        sink(tile + warp * (32 * R) + q * 32 + lane, kr[q], ki[q], rk[q], is1 ? 1 : 2,
+             f1 + __popc(b1[q] & lt), f2 + __popc(b2[q] & lt));
+      f1 += __popc(b1[q]);
+      f2 += __popc(b2[q]);
     }
-    fronts_seen += tf;
-    ties_seen += tt;
+    seen1 += t1;
+    seen2 += t2;
     buf ^= 1;
   }
-  return make_uint2(fronts_seen, ties_seen);
+  __syncthreads(); // sink writes visible; scan_tot free for the next walk
+  return make_uint2(seen1, seen2);
 }
 
 // Block-wide maximum of a rank value (every thread gets the result).
@@ -220,7 +260,6 @@ template <class Rank, int NT>
 __device__ __forceinline__ Rank block_max(Ctrl& ctl, Rank v)
 {
   v = warp_max(v);
-  __syncthreads(); // ctl.red may still be read by a previous reduction
   if (lane_id() == 0)
     ctl.red[threadIdx.x >> 5] = (uint64_t)v;
   __syncthreads();
@@ -230,30 +269,34 @@ __device__ __forceinline__ Rank block_max(Ctrl& ctl, Rank v)
     const Rank x = (Rank)ctl.red[w];
     m = x > m ? x : m;
   }
+  __syncthreads(); // ctl.red is free again
   return m;
 }
 
-// In-place trim of the list to its kk best entries, keeping list order.
-// Returns the largest rank kept (the new acceptance bound).
+// In-place trim of the list to its kk best entries (count > kk > 0).
+// Returns the largest rank kept: later keys (which come after every kept one
+// in preference order) are accepted only below it.
 template <class TR, int NT>
 __device__ __noinline__ typename TR::Rank trim_list(Ctrl& ctl, typename TR::Raw* raw, uint32_t* idx,
-                                       uint32_t count, uint32_t kk, typename TR::Rank dirmask)
+                                                    uint32_t count, uint32_t kk, typename TR::Rank dirmask,
+                                                    bool prefer_larger)
 {
   using Raw = typename TR::Raw;
   using Rank = typename TR::Rank;
-  const Selection<Rank> s = block_select<TR, NT>(ctl, raw, count, kk, dirmask);
+  const Selection<Rank> s = block_select<TR, NT>(ctl, raw, idx, count, kk, dirmask, prefer_larger);
   Rank mx = 0;
-  const uint32_t ties = s.ties;
-  scan_list<TR, NT>(ctl, raw, idx, count, dirmask, s.prefix, s.mask,
-                    [&](uint32_t, Raw kr, uint32_t ki, Rank rk, bool isf, uint32_t fr, uint32_t tr) {
-                      if (isf || tr < ties) {
-                        const uint32_t pos = fr + (tr < ties ? tr : ties);
-                        raw[pos] = kr;
-                        idx[pos] = ki;
-                        mx = rk > mx ? rk : mx;
-                      }
-                    });
-  return block_max<Rank, NT>(ctl, mx); // its barriers also publish the compacted list
+  scan_list<TR, NT>(
+    ctl, raw, idx, count, dirmask,
+    [&](uint32_t, Raw, uint32_t ki, Rank rk) { return s.classify(rk, pref_index(ki, prefer_larger)); },
+    [&](uint32_t, Raw kr, uint32_t ki, Rank rk, int, uint32_t r1, uint32_t r2) {
+      const uint32_t pos = r1 + r2;
+      raw[pos] = kr;
+      idx[pos] = ki;
+      mx = rk > mx ? rk : mx;
+    });
+  if (threadIdx.x == 0)
+    ctl.list_count = kk;
+  return block_max<Rank, NT>(ctl, mx);
 }
 
 // ---------------------------------------------------------------------------
@@ -325,14 +368,14 @@ __host__ __device__ inline uint32_t sort_scratch_bytes(uint32_t m, int rank_bits
 }
 
 // Sort the m items (raw[i], idx[i]) (i < m) and write them to the output
-// slots of one segment. `scratch` must hold sort_scratch_bytes(m) bytes.
+// slots of one segment. `scratch` must hold sort_scratch_bytes(m) bytes and
+// the items must be visible to the whole block.
 template <class TR, int NT>
 __device__ __noinline__ void sort_and_write(const typename TR::Raw* raw, const uint32_t* idx, uint32_t m,
-                               typename TR::Rank dirmask, unsigned char* scratch,
-                               typename TR::Raw* out_keys, int32_t* out_values,
-                               const int32_t* values)
+                                            typename TR::Rank dirmask, unsigned char* scratch,
+                                            typename TR::Raw* out_keys, int32_t* out_values,
+                                            const int32_t* values)
 {
-  using Rank = typename TR::Rank;
   const uint32_t n2 = next_pow2(m < 2 ? 2 : m);
   if constexpr (TR::kRankBits <= 32) {
     uint64_t* key = reinterpret_cast<uint64_t*>(scratch);

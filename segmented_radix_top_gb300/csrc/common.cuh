@@ -2,10 +2,12 @@
 //
 // Inline PTX for: 1-D bulk copies (TMA) driven by mbarriers, thread-block
 // cluster barriers and distributed shared memory (DSMEM) access, plus the
-// order-preserving key transform.
+// order-preserving key transform and its raw-domain superset filter.
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace segtopk {
@@ -128,6 +130,15 @@ __device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v)
 {
   asm volatile("red.relaxed.cluster.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v)
+{
+  uint32_t old;
+  asm volatile("atom.relaxed.cluster.shared::cluster.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "r"(addr), "r"(v)
+               : "memory");
+  return old;
+}
 __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr)
 {
   uint32_t v;
@@ -162,12 +173,45 @@ __device__ __forceinline__ void dsmem_st(uint32_t addr, uint64_t v)
 // better key. XOR-ing every bit reverses every radix digit, i.e. the bucket
 // index b becomes num_buckets-1-b for the max direction -- the bucket
 // reversal of the same page's Fix section -- and the raw key bits are only
-// ever copied, never compared.
+// ever copied, never compared as ranks.
+//
+// Each key kind provides
+//   rank(x, dirmask)       the rank code (smaller = better);
+//   unrank(r, dirmask)     raw bits of a key with rank r (never -0.0);
+//   may_pass(v, b, is_max) for a 16-byte vector of keys: false only if no
+//                          key in it can rank below the bound b (rank b.tau,
+//                          raw bits b.raw). It may answer true for keys that
+//                          then fail the exact rank test (ties, NaNs), never
+//                          false for one that passes. Floats use one native
+//                          compare per key ("not worse than the bound", which
+//                          is also true for NaN), integers the exact test.
 // ---------------------------------------------------------------------------
 enum class KeyKind : int { F16 = 0, BF16 = 1, F32 = 2, F64 = 3, U32 = 4, I32 = 5 };
 
+template <class Raw, class Rank>
+struct Bound {
+  Rank tau; // accept a key iff its rank is below tau
+  Raw raw;  // bits of a key whose rank is tau
+};
+
 template <KeyKind K>
 struct KeyTraits;
+
+// IEEE floats of 16, 32 or 64 bits.
+template <class Raw, int BITS>
+struct FloatRank {
+  static constexpr Raw kSign = (Raw)((Raw)1 << (BITS - 1));
+  __device__ __forceinline__ static Raw t(Raw x)
+  {
+    const Raw v = (x == kSign) ? (Raw)0 : x; // -0.0 -> +0.0
+    const Raw neg = (Raw)((Raw)0 - (Raw)(v >> (BITS - 1)));
+    return (Raw)(v ^ (Raw)(neg | kSign));
+  }
+  __device__ __forceinline__ static Raw t_inv(Raw t)
+  {
+    return (t & kSign) ? (Raw)(t & (Raw)~kSign) : (Raw)~t;
+  }
+};
 
 template <>
 struct KeyTraits<KeyKind::F16> {
@@ -176,24 +220,71 @@ struct KeyTraits<KeyKind::F16> {
   static constexpr int kRankBits = 16;
   __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask)
   {
-    uint32_t v = (x == 0x8000u) ? 0u : x;
-    uint32_t neg = 0u - (v >> 15);
-    return ((v ^ (neg | 0x8000u)) & 0xffffu) ^ dirmask;
+    return ((Rank)FloatRank<uint16_t, 16>::t(x)) ^ dirmask;
+  }
+  __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask)
+  {
+    return FloatRank<uint16_t, 16>::t_inv((uint16_t)(r ^ dirmask));
+  }
+  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  {
+    const __half e = __ushort_as_half(b.raw);
+    const __half2 h = __halves2half2(e, e);
+    const __half2* w = reinterpret_cast<const __half2*>(&v);
+    unsigned m;
+    if (is_max)
+      m = __hgeu2_mask(w[0], h) | __hgeu2_mask(w[1], h) | __hgeu2_mask(w[2], h) | __hgeu2_mask(w[3], h);
+    else
+      m = __hleu2_mask(w[0], h) | __hleu2_mask(w[1], h) | __hleu2_mask(w[2], h) | __hleu2_mask(w[3], h);
+    return m != 0;
   }
 };
+
 template <>
-struct KeyTraits<KeyKind::BF16> : KeyTraits<KeyKind::F16> {};
+struct KeyTraits<KeyKind::BF16> {
+  using Raw = uint16_t;
+  using Rank = uint32_t;
+  static constexpr int kRankBits = 16;
+  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask)
+  {
+    return ((Rank)FloatRank<uint16_t, 16>::t(x)) ^ dirmask;
+  }
+  __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask)
+  {
+    return FloatRank<uint16_t, 16>::t_inv((uint16_t)(r ^ dirmask));
+  }
+  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  {
+    const __nv_bfloat16 e = __ushort_as_bfloat16(b.raw);
+    const __nv_bfloat162 h = __halves2bfloat162(e, e);
+    const __nv_bfloat162* w = reinterpret_cast<const __nv_bfloat162*>(&v);
+    unsigned m;
+    if (is_max)
+      m = __hgeu2_mask(w[0], h) | __hgeu2_mask(w[1], h) | __hgeu2_mask(w[2], h) | __hgeu2_mask(w[3], h);
+    else
+      m = __hleu2_mask(w[0], h) | __hleu2_mask(w[1], h) | __hleu2_mask(w[2], h) | __hleu2_mask(w[3], h);
+    return m != 0;
+  }
+};
 
 template <>
 struct KeyTraits<KeyKind::F32> {
   using Raw = uint32_t;
   using Rank = uint32_t;
   static constexpr int kRankBits = 32;
-  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask)
+  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return FloatRank<uint32_t, 32>::t(x) ^ dirmask; }
+  __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask)
   {
-    uint32_t v = (x == 0x80000000u) ? 0u : x;
-    uint32_t neg = 0u - (v >> 31);
-    return (v ^ (neg | 0x80000000u)) ^ dirmask;
+    return FloatRank<uint32_t, 32>::t_inv(r ^ dirmask);
+  }
+  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  {
+    const float f = __uint_as_float(b.raw);
+    const float x0 = __uint_as_float(v.x), x1 = __uint_as_float(v.y);
+    const float x2 = __uint_as_float(v.z), x3 = __uint_as_float(v.w);
+    if (is_max)
+      return !(x0 < f) || !(x1 < f) || !(x2 < f) || !(x3 < f);
+    return !(x0 > f) || !(x1 > f) || !(x2 > f) || !(x3 > f);
   }
 };
 
@@ -202,11 +293,24 @@ struct KeyTraits<KeyKind::F64> {
   using Raw = uint64_t;
   using Rank = uint64_t;
   static constexpr int kRankBits = 64;
-  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask)
+  __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return FloatRank<uint64_t, 64>::t(x) ^ dirmask; }
+  __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask)
   {
-    uint64_t v = (x == 0x8000000000000000ull) ? 0ull : x;
-    uint64_t neg = 0ull - (v >> 63);
-    return (v ^ (neg | 0x8000000000000000ull)) ^ dirmask;
+    return FloatRank<uint64_t, 64>::t_inv(r ^ dirmask);
+  }
+  // the exact high 32 bits of a key's rank, from its two words
+  __device__ __forceinline__ static uint32_t rank_hi(uint32_t lo, uint32_t hi, uint32_t dm_hi)
+  {
+    if (hi == 0x80000000u && lo == 0u)
+      hi = 0u; // -0.0
+    return (hi ^ ((hi & 0x80000000u) ? 0xffffffffu : 0x80000000u)) ^ dm_hi;
+  }
+  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  {
+    // rank < tau implies rank_hi <= tau_hi: a superset test on one word
+    const uint32_t dm_hi = is_max ? 0xffffffffu : 0u;
+    const uint32_t th = (uint32_t)(b.tau >> 32);
+    return rank_hi(v.x, v.y, dm_hi) <= th || rank_hi(v.z, v.w, dm_hi) <= th;
   }
 };
 
@@ -216,6 +320,12 @@ struct KeyTraits<KeyKind::U32> {
   using Rank = uint32_t;
   static constexpr int kRankBits = 32;
   __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return x ^ dirmask; }
+  __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask) { return r ^ dirmask; }
+  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  {
+    const uint32_t dm = is_max ? 0xffffffffu : 0u; // exact
+    return (v.x ^ dm) < b.tau || (v.y ^ dm) < b.tau || (v.z ^ dm) < b.tau || (v.w ^ dm) < b.tau;
+  }
 };
 
 template <>
@@ -224,6 +334,12 @@ struct KeyTraits<KeyKind::I32> {
   using Rank = uint32_t;
   static constexpr int kRankBits = 32;
   __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return (x ^ 0x80000000u) ^ dirmask; }
+  __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask) { return (r ^ dirmask) ^ 0x80000000u; }
+  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  {
+    const uint32_t dm = (is_max ? 0xffffffffu : 0u) ^ 0x80000000u; // exact
+    return (v.x ^ dm) < b.tau || (v.y ^ dm) < b.tau || (v.z ^ dm) < b.tau || (v.w ^ dm) < b.tau;
+  }
 };
 
 // ---------------------------------------------------------------------------
