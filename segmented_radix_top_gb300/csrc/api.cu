@@ -68,34 +68,32 @@ cudaError_t device_info(DeviceInfo* out)
   return cudaSuccess;
 }
 
-constexpr uint32_t kStages = 4;
+constexpr uint32_t kStages = 2;
 constexpr int64_t kMinSliceKeys = 16384; // a CTA of a multi-CTA cluster reads at least this many keys
 constexpr int kThreads = 256;
 
 struct Plan {
   LaunchShape shape;
   uint32_t list_cap;
-  uint32_t trim_at;
   uint32_t ring_bytes;
   bool merge_gather;
 };
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Candidate-list slack: entries appended after a trim before the next one.
-constexpr uint32_t kListSlack = 512;
+// Candidate-list room beyond k: keys accepted after a selection before the
+// list overflows and the next selection (over the list and the chunk being
+// read) tightens the bound.
+uint32_t list_slack(uint32_t k) { return std::max(512u, k / 2); }
 
-// Shared-memory sizing for a given k and cluster width. The list must absorb
-// a whole chunk after reaching the trim threshold; the ring doubles as sort
-// scratch and, in a cluster leader, as gather space.
+// Shared-memory sizing for a given k and cluster width. The ring doubles as
+// sort scratch and, in a cluster leader, as gather space.
 Plan size_plan(const KeyOps& ops, int32_t k, int cluster)
 {
   Plan pl;
   const uint32_t kb = (uint32_t)ops.key_bytes;
-  const uint32_t chunk_keys = kChunkBytes / kb;
   const uint32_t uk = (uint32_t)k;
-  pl.list_cap = align_up(uk + chunk_keys + kListSlack, 32);
-  pl.trim_at = pl.list_cap - chunk_keys;
+  pl.list_cap = align_up(uk + list_slack(uk), 32);
   const uint32_t stream_ring = kStages * kChunkBytes;
   const uint32_t sort_need = sort_scratch_bytes(uk, ops.rank_bits);
   uint32_t need = sort_need;
@@ -109,7 +107,7 @@ Plan size_plan(const KeyOps& ops, int32_t k, int cluster)
   pl.ring_bytes = align_up(std::max(stream_ring, need), 128);
   pl.shape.threads = kThreads;
   pl.shape.cluster = cluster;
-  pl.shape.smem = kCtrlBytes + pl.ring_bytes + list_bytes(pl.list_cap, kb);
+  pl.shape.smem = kCtrlBytes + pl.ring_bytes + list_bytes(pl.list_cap, kb) + kCandBytes;
   return pl;
 }
 
@@ -311,7 +309,6 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
     p.dirmask &= 0xffffffffull;
   p.k = k;
   p.list_cap = pl.list_cap;
-  p.trim_at = pl.trim_at;
   p.merge_gather = pl.merge_gather ? 1 : 0;
   p.ring_stages = kStages;
   p.ring_bytes = pl.ring_bytes;

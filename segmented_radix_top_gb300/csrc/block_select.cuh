@@ -26,12 +26,33 @@ struct Ctrl {
   uint32_t hist[2][kBuckets];     // digit histograms (double buffered; zero outside a selection)
   uint32_t hist_merged[kBuckets]; // cluster leader: histogram pushed by the other CTAs
   uint32_t res[4];                // selection result of a pass: bucket, count before, bucket count
-  uint32_t list_count;            // entries in the candidate list
+  uint32_t chunk_count[3];        // entries appended during a chunk (three in rotation)
   uint32_t gather_count;          // cluster leader: entries gathered from the cluster
   uint32_t front_base;            // cross-CTA scan: selected entries of preceding CTAs
   uint32_t tie_base;              // cross-CTA scan: boundary ties of preceding CTAs
 };
 constexpr uint32_t kCtrlBytes = (sizeof(Ctrl) + 127u) & ~127u;
+
+// Entries a selection reads: `count` list entries, then `ext_count` keys of
+// a ring stage whose source indices are ext_idx0, ext_idx0 + 1, ...
+template <class Raw>
+struct Src {
+  const Raw* raw;
+  const uint32_t* idx;
+  uint32_t count;
+  const Raw* ext_raw;
+  uint32_t ext_idx0;
+  uint32_t ext_count;
+  __device__ __forceinline__ uint32_t size() const { return count + ext_count; }
+  __device__ __forceinline__ Raw key(uint32_t e) const { return e < count ? raw[e] : ext_raw[e - count]; }
+  __device__ __forceinline__ uint32_t index(uint32_t e) const { return e < count ? idx[e] : ext_idx0 + (e - count); }
+};
+
+template <class Raw>
+__device__ __forceinline__ Src<Raw> list_src(const Raw* raw, const uint32_t* idx, uint32_t count)
+{
+  return Src<Raw>{raw, idx, count, nullptr, 0u, 0u};
+}
 
 // Warp 0 of the block: find the bucket holding the krem-th best candidate.
 // `h` holds the 8 bucket counts this lane owns (buckets 8*lane .. 8*lane+7).
@@ -72,30 +93,117 @@ struct Radix {
   bool stopped;    // the boundary bucket held exactly krem candidates
 };
 
-// One radix selection over list entries [0, count): among the candidates
-// (get(e, key) returns true), find the kk best by key (smaller = better).
-// Each pass histograms one 8-bit digit of the candidates whose resolved
-// digits match, finds the bucket holding the krem-th best, narrows krem and
-// folds the digit into the prefix; it stops when that bucket holds exactly
-// krem candidates ("Implement Segmented TopK using Thread-Block-Clusters",
-// sections 1.2 "Radix (digit) top-k" and 1.4 "Early stop").
-// Requires count >= kk > 0 candidates. Block-wide; leaves both histograms zero.
+// Candidate-position buffer (shared memory) that a selection may use to
+// visit only the boundary candidates after its first two passes.
+struct CandBuf {
+  uint16_t* pos;  // entry positions (an entry domain is < 65536 entries)
+  uint32_t cap;
+  uint32_t n;     // filled by radix_select: candidates stored, or ~0u if not compacted
+};
+
+// Warp-wide AND / OR of the keys of the lanes where `on` holds, folded into
+// shared words with native 32-bit atomics (one pair per warp and word).
+__device__ __forceinline__ void warp_and_or(uint32_t* a, uint32_t* o, bool on, uint32_t v)
+{
+  const uint32_t wa = __reduce_and_sync(kFull, on ? v : ~0u);
+  const uint32_t wo = __reduce_or_sync(kFull, on ? v : 0u);
+  if (lane_id() == 0) {
+    atomicAnd(a, wa);
+    atomicOr(o, wo);
+  }
+}
+__device__ __forceinline__ void warp_and_or(uint32_t* a, uint32_t* o, bool on, uint64_t v)
+{
+  warp_and_or(a, o, on, (uint32_t)v);
+  warp_and_or(a + 1, o + 1, on, (uint32_t)(v >> 32));
+}
+
+// One radix selection: among the candidates (get(e, key) returns true) of
+// the entries e of a domain -- [0, count), or the positions dom[0..dom_n) if
+// dom is given -- find the kk best by key (smaller = better). Each pass
+// histograms one 8-bit digit of the candidates whose resolved digits match,
+// finds the bucket holding the krem-th best, narrows krem and folds the digit
+// into the prefix; it stops when that bucket holds exactly krem candidates
+// ("Implement Segmented TopK using Thread-Block-Clusters", sections 1.2
+// "Radix (digit) top-k" and 1.4 "Early stop").
+//
+// Work saving: the second pass also stores the positions of the remaining
+// candidates in `cb` (when they fit) and the AND / OR of their keys; later
+// passes then visit only those positions, and a digit on which all of them
+// agree is folded without a pass.
+// Requires at least kk candidates. Block-wide; leaves both histograms zero.
 template <class Key, int KEY_BITS, int NT, class Get>
-__device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, uint32_t kk, Get&& get)
+__device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* dom, uint32_t dom_n,
+                                   uint32_t kk, CandBuf& cb, Get&& get)
 {
   constexpr int P = KEY_BITS / kDigitBits;
   Radix<Key> r{(Key)0, (Key)0, kk, false};
-  int p = 0;
-  for (; p < P; ++p) {
+  uint32_t* kand = reinterpret_cast<uint32_t*>(&ctl.red[0]); // AND of candidate keys (1 or 2 words)
+  uint32_t* kor = reinterpret_cast<uint32_t*>(&ctl.red[1]);  // OR of candidate keys
+  const uint32_t span = dom ? dom_n : count;
+  uint32_t* ncand = &ctl.res[3];
+  bool compacted = false;
+  Key diff = ~(Key)0; // digits that differ among the candidates (all, until known)
+  Key kand_v = 0;
+  int hb = 0; // histogram buffer of the current pass
+  for (int p = 0; p < P; ++p) {
     const int shift = KEY_BITS - kDigitBits * (p + 1);
-    uint32_t* h = ctl.hist[p & 1];
-    for (uint32_t e = threadIdx.x; e < count; e += NT) {
-      Key key;
-      if (get(e, key) && (key & r.mask) == r.prefix)
-        atomicAdd(&h[(uint32_t)(key >> shift) & (kBuckets - 1)], 1u);
+    const Key dmask = (Key)(kBuckets - 1) << shift;
+    if (p >= 2 && !(diff & dmask)) {
+      // every candidate has the same digit here: fold it without a pass
+      r.prefix |= kand_v & dmask;
+      r.mask |= dmask;
+      continue;
+    }
+    uint32_t* h = ctl.hist[hb];
+    const bool collect = p == 1 && cb.pos != nullptr;
+    if (compacted) {
+      const uint32_t nc = *ncand;
+      for (uint32_t i = threadIdx.x; i < nc; i += NT) {
+        Key key;
+        const uint32_t e = cb.pos[i];
+        if (get(e, key) && (key & r.mask) == r.prefix)
+          atomicAdd(&h[(uint32_t)(key >> shift) & (kBuckets - 1)], 1u);
+      }
+    } else if (!collect) {
+      for (uint32_t i = threadIdx.x; i < span; i += NT) {
+        Key key;
+        const uint32_t e = dom ? dom[i] : i;
+        if (get(e, key) && (key & r.mask) == r.prefix)
+          atomicAdd(&h[(uint32_t)(key >> shift) & (kBuckets - 1)], 1u);
+      }
+    } else {
+      // uniform trip count: the warp-wide ballots and reductions need every lane
+      for (uint32_t base = 0; base < span; base += NT) {
+        const uint32_t i = base + threadIdx.x;
+        Key key = 0;
+        uint32_t e = 0;
+        bool on = false;
+        if (i < span) {
+          e = dom ? dom[i] : i;
+          on = get(e, key) && (key & r.mask) == r.prefix;
+        }
+        if (on)
+          atomicAdd(&h[(uint32_t)(key >> shift) & (kBuckets - 1)], 1u);
+        const uint32_t bal = __ballot_sync(kFull, on);
+        if (bal) {
+          uint32_t slot = 0;
+          if (lane_id() == 0)
+            slot = atomicAdd(ncand, __popc(bal));
+          slot = __shfl_sync(kFull, slot, 0) + __popc(bal & lanemask_lt());
+          if (on && slot < cb.cap)
+            cb.pos[slot] = (uint16_t)e;
+          warp_and_or(kand, kor, on, key);
+        }
+      }
     }
     if (threadIdx.x < kBuckets)
-      ctl.hist[(p + 1) & 1][threadIdx.x] = 0;
+      ctl.hist[hb ^ 1][threadIdx.x] = 0;
+    if (threadIdx.x == 0 && p == 0 && cb.pos != nullptr) {
+      *ncand = 0;
+      kand[0] = kand[1] = ~0u;
+      kor[0] = kor[1] = 0u;
+    }
     __syncthreads();
     if (threadIdx.x < 32) {
       uint32_t hh[8];
@@ -106,20 +214,33 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, uint32_t kk, Get&&
     }
     __syncthreads();
     const uint32_t b = ctl.res[0], before = ctl.res[1], cnt = ctl.res[2];
+    if (collect) {
+      compacted = *ncand <= cb.cap;
+      Key a, o;
+      if constexpr (sizeof(Key) == 8) {
+        a = ((Key)kand[1] << 32) | kand[0];
+        o = ((Key)kor[1] << 32) | kor[0];
+      } else {
+        a = (Key)kand[0];
+        o = (Key)kor[0];
+      }
+      kand_v = a;
+      diff = a ^ o;
+    }
     r.krem -= before;
     r.prefix |= (Key)b << shift;
-    r.mask |= (Key)(kBuckets - 1) << shift;
+    r.mask |= dmask;
+    if (threadIdx.x < kBuckets)
+      h[threadIdx.x] = 0; // warp 0 read it before the barrier above
+    hb ^= 1;
     if (cnt == r.krem) {
       r.stopped = true;
       break;
     }
+    // ctl.res, the candidate count and h are rewritten only after the next barrier
   }
-  if (p == P)
-    p = P - 1;
-  // restore the "both histograms zero" invariant (warp 0 read this one before the last barrier)
-  if (threadIdx.x < kBuckets)
-    ctl.hist[p & 1][threadIdx.x] = 0;
-  __syncthreads(); // ctl.res may be rewritten by the next selection
+  cb.n = compacted ? *ncand : ~0u;
+  __syncthreads(); // histograms zero and ctl.res / ctl.red free for the next selection
   return r;
 }
 
@@ -149,38 +270,43 @@ struct Selection {
 
 // Boundary ties by source index: among entries with (rank & mask) == prefix,
 // choose the q preferred ones (0 < q < their count) by a second radix
-// selection on the preference index, which is unique within a segment.
+// selection on the preference index, which is unique within a segment. If
+// the rank selection left the boundary candidates in `cb`, only those are
+// visited.
 template <class TR, int NT>
-__device__ void select_ties(Ctrl& ctl, const typename TR::Raw* raw, const uint32_t* idx, uint32_t count,
-                            uint32_t q, typename TR::Rank dirmask, bool prefer_larger,
-                            Selection<typename TR::Rank>& s)
+__device__ void select_ties(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_t q,
+                            typename TR::Rank dirmask, bool prefer_larger, Selection<typename TR::Rank>& s,
+                            CandBuf& cb)
 {
   using Rank = typename TR::Rank;
   const Rank prefix = s.prefix, mask = s.mask;
-  const Radix<uint32_t> ri = radix_select<uint32_t, 32, NT>(ctl, count, q, [&](uint32_t e, uint32_t& key) {
-    key = pref_index(idx[e], prefer_larger);
-    return (TR::rank(raw[e], dirmask) & mask) == prefix;
-  });
+  const bool use = cb.pos != nullptr && cb.n != ~0u;
+  CandBuf none{nullptr, 0u, ~0u};
+  const Radix<uint32_t> ri = radix_select<uint32_t, 32, NT>(
+    ctl, src.size(), use ? cb.pos : nullptr, use ? cb.n : 0u, q, use ? none : cb, [&](uint32_t e, uint32_t& key) {
+      key = pref_index(src.index(e), prefer_larger);
+      return (TR::rank(src.key(e), dirmask) & mask) == prefix;
+    });
   s.iprefix = ri.prefix;
   s.imask = ri.mask;
 }
 
-// The kk best of `count` list entries (count > kk > 0) in one CTA: a radix
+// The kk best of the entries of `src` (size > kk > 0) in one CTA: a radix
 // selection on the rank code, then, if more boundary entries tie than are
 // needed, one on the preference index.
 template <class TR, int NT>
-__device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, const typename TR::Raw* raw,
-                                                     const uint32_t* idx, uint32_t count, uint32_t kk,
-                                                     typename TR::Rank dirmask, bool prefer_larger)
+__device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_t kk,
+                                                     typename TR::Rank dirmask, bool prefer_larger, CandBuf cb)
 {
   using Rank = typename TR::Rank;
-  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, count, kk, [&](uint32_t e, Rank& key) {
-    key = TR::rank(raw[e], dirmask);
-    return true;
-  });
+  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, src.size(), nullptr, 0u, kk, cb,
+                                                               [&](uint32_t e, Rank& key) {
+                                                                 key = TR::rank(src.key(e), dirmask);
+                                                                 return true;
+                                                               });
   Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u};
   if (!rr.stopped) // every rank digit resolved and more than krem entries share the boundary rank
-    select_ties<TR, NT>(ctl, raw, idx, count, rr.krem, dirmask, prefer_larger, s);
+    select_ties<TR, NT>(ctl, src, rr.krem, dirmask, prefer_larger, s, cb);
   return s;
 }
 
@@ -193,9 +319,10 @@ __device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, const typename T
 // follows every thread's reads of the current tile, so it may overwrite list
 // slots at or before the tile.
 template <class TR, int NT, class Classify, class Sink>
-__device__ uint2 scan_list(Ctrl& ctl, const typename TR::Raw* raw, const uint32_t* idx, uint32_t count,
-                           typename TR::Rank dirmask, Classify&& classify, Sink&& sink)
+__device__ uint2 scan_list(Ctrl& ctl, const Src<typename TR::Raw>& src, typename TR::Rank dirmask,
+                           Classify&& classify, Sink&& sink)
 {
+  const uint32_t count = src.size();
   using Raw = typename TR::Raw;
   using Rank = typename TR::Rank;
   constexpr int NW = NT / 32;
@@ -214,8 +341,8 @@ __device__ uint2 scan_list(Ctrl& ctl, const typename TR::Raw* raw, const uint32_
     for (int q = 0; q < R; ++q) {
       const uint32_t e = tile + warp * (32 * R) + q * 32 + lane;
       const bool valid = e < count;
-      kr[q] = valid ? raw[e] : Raw(0);
-      ki[q] = valid ? idx[e] : 0u;
+      kr[q] = valid ? src.key(e) : Raw(0);
+      ki[q] = valid ? src.index(e) : 0u;
       rk[q] = TR::rank(kr[q], dirmask);
       const int c = valid ? classify(e, kr[q], ki[q], rk[q]) : 0;
       b1[q] = __ballot_sync(kFull, c == 1);
@@ -273,29 +400,29 @@ __device__ __forceinline__ Rank block_max(Ctrl& ctl, Rank v)
   return m;
 }
 
-// In-place trim of the list to its kk best entries (count > kk > 0).
-// Returns the largest rank kept: later keys (which come after every kept one
-// in preference order) are accepted only below it.
+// Keep the kk best entries of `src` (size > kk > 0), written to dst[0, kk)
+// in their order in src. dst may be src's list arrays: every entry is written
+// at or before its own position, after its tile has been read. Returns the
+// largest rank kept: later keys (which come after every kept one in
+// preference order) are accepted only below it.
 template <class TR, int NT>
-__device__ __noinline__ typename TR::Rank trim_list(Ctrl& ctl, typename TR::Raw* raw, uint32_t* idx,
-                                                    uint32_t count, uint32_t kk, typename TR::Rank dirmask,
-                                                    bool prefer_larger)
+__device__ __noinline__ typename TR::Rank trim_into(Ctrl& ctl, const Src<typename TR::Raw> src,
+                                                    typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t kk,
+                                                    typename TR::Rank dirmask, bool prefer_larger, CandBuf cb)
 {
   using Raw = typename TR::Raw;
   using Rank = typename TR::Rank;
-  const Selection<Rank> s = block_select<TR, NT>(ctl, raw, idx, count, kk, dirmask, prefer_larger);
+  const Selection<Rank> s = block_select<TR, NT>(ctl, src, kk, dirmask, prefer_larger, cb);
   Rank mx = 0;
   scan_list<TR, NT>(
-    ctl, raw, idx, count, dirmask,
+    ctl, src, dirmask,
     [&](uint32_t, Raw, uint32_t ki, Rank rk) { return s.classify(rk, pref_index(ki, prefer_larger)); },
     [&](uint32_t, Raw kr, uint32_t ki, Rank rk, int, uint32_t r1, uint32_t r2) {
       const uint32_t pos = r1 + r2;
-      raw[pos] = kr;
-      idx[pos] = ki;
+      dst_raw[pos] = kr;
+      dst_idx[pos] = ki;
       mx = rk > mx ? rk : mx;
     });
-  if (threadIdx.x == 0)
-    ctl.list_count = kk;
   return block_max<Rank, NT>(ctl, mx);
 }
 

@@ -283,8 +283,8 @@ struct KeyTraits<KeyKind::F32> {
     const float x0 = __uint_as_float(v.x), x1 = __uint_as_float(v.y);
     const float x2 = __uint_as_float(v.z), x3 = __uint_as_float(v.w);
     if (is_max)
-      return !(x0 < f) || !(x1 < f) || !(x2 < f) || !(x3 < f);
-    return !(x0 > f) || !(x1 > f) || !(x2 > f) || !(x3 > f);
+      return !(x0 < f) | !(x1 < f) | !(x2 < f) | !(x3 < f);
+    return !(x0 > f) | !(x1 > f) | !(x2 > f) | !(x3 > f);
   }
 };
 
@@ -310,7 +310,7 @@ struct KeyTraits<KeyKind::F64> {
     // rank < tau implies rank_hi <= tau_hi: a superset test on one word
     const uint32_t dm_hi = is_max ? 0xffffffffu : 0u;
     const uint32_t th = (uint32_t)(b.tau >> 32);
-    return rank_hi(v.x, v.y, dm_hi) <= th || rank_hi(v.z, v.w, dm_hi) <= th;
+    return (rank_hi(v.x, v.y, dm_hi) <= th) | (rank_hi(v.z, v.w, dm_hi) <= th);
   }
 };
 
@@ -324,7 +324,7 @@ struct KeyTraits<KeyKind::U32> {
   __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
   {
     const uint32_t dm = is_max ? 0xffffffffu : 0u; // exact
-    return (v.x ^ dm) < b.tau || (v.y ^ dm) < b.tau || (v.z ^ dm) < b.tau || (v.w ^ dm) < b.tau;
+    return ((v.x ^ dm) < b.tau) | ((v.y ^ dm) < b.tau) | ((v.z ^ dm) < b.tau) | ((v.w ^ dm) < b.tau);
   }
 };
 
@@ -338,7 +338,7 @@ struct KeyTraits<KeyKind::I32> {
   __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
   {
     const uint32_t dm = (is_max ? 0xffffffffu : 0u) ^ 0x80000000u; // exact
-    return (v.x ^ dm) < b.tau || (v.y ^ dm) < b.tau || (v.z ^ dm) < b.tau || (v.w ^ dm) < b.tau;
+    return ((v.x ^ dm) < b.tau) | ((v.y ^ dm) < b.tau) | ((v.z ^ dm) < b.tau) | ((v.w ^ dm) < b.tau);
   }
 };
 

@@ -33,7 +33,7 @@
 
 namespace segtopk {
 
-constexpr uint32_t kChunkBytes = 16384;
+constexpr uint32_t kChunkBytes = 32768;
 
 struct KernelParams {
   const void* keys;
@@ -47,7 +47,6 @@ struct KernelParams {
   uint64_t dirmask;      // rank = T(key) ^ dirmask: all ones for max, zero for min
   int32_t k;
   uint32_t list_cap;     // candidate list capacity (entries)
-  uint32_t trim_at;      // trim when the list holds more than this after a chunk
   uint32_t ring_stages;  // pipeline depth (<= 8)
   uint32_t ring_bytes;   // ring region bytes (also sort / gather scratch)
   int32_t prefer_larger; // tie preference: larger source index first
@@ -62,6 +61,11 @@ __host__ __device__ inline uint32_t list_bytes(uint32_t cap, uint32_t key_bytes)
 {
   return align16(cap * key_bytes) + cap * 4u;
 }
+// Keys of the first chunk used to form the first bound.
+constexpr uint32_t kBootKeys = 2048;
+// Candidate positions kept by a selection between its passes.
+constexpr uint32_t kCandCap = 8192;
+constexpr uint32_t kCandBytes = kCandCap * 2u;
 
 template <KeyKind KK, int NT>
 __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p)
@@ -73,12 +77,15 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   constexpr int U = (int)kChunkBytes / 16 / NT; // vectors per thread per chunk
   constexpr uint32_t kChunkVec = kChunkBytes / 16;
   static_assert(U >= 1 && U <= 8, "chunk / thread configuration");
+  static_assert(kChunkBytes / sizeof(Raw) >= NT, "a chunk gives every thread keys");
 
   extern __shared__ __align__(128) unsigned char smem[];
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem);
   unsigned char* ring = smem + kCtrlBytes;
   Raw* list_raw = reinterpret_cast<Raw*>(ring + p.ring_bytes);
   uint32_t* list_idx = reinterpret_cast<uint32_t*>(ring + p.ring_bytes + align16(p.list_cap * sizeof(Raw)));
+  uint16_t* cand_pos = reinterpret_cast<uint16_t*>(ring + p.ring_bytes + list_bytes(p.list_cap, sizeof(Raw)));
+  const CandBuf cbuf{cand_pos, kCandCap, 0u};
 
   const uint32_t C = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
@@ -110,7 +117,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
     ctl.hist_merged[i] = 0;
   }
   if (threadIdx.x == 0) {
-    ctl.list_count = 0;
+    ctl.chunk_count[0] = ctl.chunk_count[1] = ctl.chunk_count[2] = 0;
     ctl.gather_count = 0;
     ctl.front_base = 0;
     ctl.tie_base = 0;
@@ -149,72 +156,188 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   }
 
   // ---- streaming selection state (uniform across the block) ----
-  bool open = true; // no bound yet: every key is accepted
+  const uint32_t L = p.list_cap;
+  uint32_t count = 0; // list entries
+  bool open = true;   // no bound yet: every key is accepted
   Bound<Raw, Rank> bound{(Rank)0, (Raw)0};
+  uint32_t step = 0;  // edges and chunks offered so far (selects the append counter)
+  const bool pl = p.prefer_larger != 0;
+
+  auto set_bound = [&](Rank tau) {
+    bound.tau = tau;
+    bound.raw = TR::unrank(tau, dirmask);
+    open = false;
+    count = k;
+  };
+  // Keep the k best of the list and `n_ext` keys at `ext` (indices idx0..).
+  auto select_union = [&](const Raw* ext, uint32_t idx0, uint32_t n_ext) {
+    set_bound(trim_into<TR, NT>(ctl, Src<Raw>{list_raw, list_idx, count, ext, idx0, n_ext}, list_raw, list_idx, k,
+                                dirmask, pl, cbuf));
+  };
 
   // Offer this thread's U vectors (vector j: vc[j] keys from slot 0, source
-  // indices i0[j] + slot) to the list. Returns true in every lane of a warp
-  // whose appends pushed the list past the trim threshold.
+  // indices i0[j] + slot). Keys that may beat the bound are tested exactly;
+  // accepted keys are appended at list positions count + (a per-lane atomic
+  // on this step's counter). Returns true if an append would overflow the
+  // list (nothing is written for that lane then).
   auto offer = [&](const uint4 (&vec)[U], const uint32_t (&vc)[U], const uint32_t (&i0)[U]) {
-    bool may = false;
+    uint32_t mayv = 0;
 #pragma unroll
     for (int j = 0; j < U; ++j)
-      if (vc[j])
-        may = may || open || TR::may_pass(vec[j], bound, is_max);
-    bool over = false;
-    if (__any_sync(kFull, may)) {
+      if (vc[j] && (open || TR::may_pass(vec[j], bound, is_max)))
+        mayv |= 1u << j;
+    bool overflow = false;
+    if (mayv) {
       uint32_t acc[U];
       uint32_t c = 0;
 #pragma unroll
       for (int j = 0; j < U; ++j) {
         acc[j] = 0;
-        if (may) {
+        if ((mayv >> j) & 1u) {
           const Raw* kv = reinterpret_cast<const Raw*>(&vec[j]);
 #pragma unroll
           for (int i = 0; i < VK; ++i)
             if ((uint32_t)i < vc[j] && (open || TR::rank(kv[i], dirmask) < bound.tau))
               acc[j] |= 1u << i;
+          c += __popc(acc[j]);
         }
-        c += __popc(acc[j]);
       }
-      const uint32_t incl = warp_inclusive_sum(c);
-      const uint32_t tot = __shfl_sync(kFull, incl, 31);
-      if (tot) {
-        uint32_t base = 0;
-        if (lane_id() == 31)
-          base = atomicAdd(&ctl.list_count, tot);
-        base = __shfl_sync(kFull, base, 31);
-        uint32_t pos = base + incl - c;
+      if (c) {
+        const uint32_t pos = count + atomicAdd(&ctl.chunk_count[step % 3], c);
+        if (pos + c > L) {
+          overflow = true;
+        } else {
+          uint32_t w = pos;
 #pragma unroll
-        for (int j = 0; j < U; ++j) {
-          const Raw* kv = reinterpret_cast<const Raw*>(&vec[j]);
+          for (int j = 0; j < U; ++j) {
+            if (acc[j]) {
+              const Raw* kv = reinterpret_cast<const Raw*>(&vec[j]);
 #pragma unroll
-          for (int i = 0; i < VK; ++i) {
-            if ((acc[j] >> i) & 1u) {
-              list_raw[pos] = kv[i];
-              list_idx[pos] = i0[j] + (uint32_t)i;
-              ++pos;
+              for (int i = 0; i < VK; ++i) {
+                if ((acc[j] >> i) & 1u) {
+                  list_raw[w] = kv[i];
+                  list_idx[w] = i0[j] + (uint32_t)i;
+                  ++w;
+                }
+              }
             }
           }
         }
-        over = base + tot > p.trim_at;
       }
     }
-    return over;
+    return overflow;
   };
 
-  // After a chunk: trim when the next chunk could overflow the list.
-  auto after_chunk = [&](bool over) {
-    const uint32_t count = ctl.list_count;
-    (void)over;
-    const Rank tau = trim_list<TR, NT>(ctl, list_raw, list_idx, count, k, dirmask, p.prefer_larger != 0);
-    bound.tau = tau;
-    bound.raw = TR::unrank(tau, dirmask);
-    open = false;
+  // After a step's barrier: account its appends (unless a selection replaced
+  // the list) and recycle the counter of the step before, which every thread
+  // read after the previous barrier; it is next used two steps from now.
+  auto finish_step = [&](bool counted) {
+    if (counted)
+      count += ctl.chunk_count[step % 3];
+    if (threadIdx.x == 0)
+      ctl.chunk_count[(step + 2) % 3] = 0;
+    ++step;
+  };
+
+  // Offer a chunk in the ring: every thread filters U vectors (may_pass);
+  // the warp then hands its candidate vectors out one per lane, so a lane
+  // re-reads one flagged vector, tests its keys exactly and appends the
+  // accepted ones. Returns true if an append would overflow the list.
+  auto offer_chunk = [&](const uint4* stage, uint32_t v0, uint32_t v1, uint32_t idx0) {
+    uint4 vv[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) // all loads first (in the ring; vectors outside [v0, v1) are masked below)
+      vv[j] = stage[(uint32_t)j * NT + threadIdx.x];
+    uint32_t mayv = 0;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const uint32_t t = (uint32_t)j * NT + threadIdx.x;
+      mayv |= (uint32_t)((t >= v0) & (t < v1) & TR::may_pass(vv[j], bound, is_max)) << j;
+    }
+    if (!__any_sync(kFull, mayv != 0))
+      return false; // the common case: nothing in this warp's share can enter the list
+    const uint32_t lane = lane_id(), warp_base = threadIdx.x & ~31u;
+    uint32_t cand[U], base[U], total = 0;
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      cand[j] = __ballot_sync(kFull, (mayv >> j) & 1u);
+      base[j] = total;
+      total += __popc(cand[j]);
+    }
+    bool overflow = false;
+    for (uint32_t b0 = 0; b0 < total; b0 += 32) {
+      const uint32_t my = b0 + lane;
+      uint32_t acc = 0, i0 = 0;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (my < total) {
+        uint32_t cj = 0, bj = 0, jj = 0;
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          if (my >= base[j] && my < base[j] + __popc(cand[j])) {
+            cj = cand[j];
+            bj = base[j];
+            jj = (uint32_t)j;
+          }
+        }
+        const uint32_t src_lane = __fns(cj, 0, (int)(my - bj) + 1);
+        const uint32_t t = jj * NT + warp_base + src_lane;
+        v = stage[t];
+        i0 = idx0 + t * VK;
+        const Raw* kv = reinterpret_cast<const Raw*>(&v);
+#pragma unroll
+        for (int i = 0; i < VK; ++i)
+          if (TR::rank(kv[i], dirmask) < bound.tau)
+            acc |= 1u << i;
+      }
+      const uint32_t c = __popc(acc);
+      if (c) {
+        const uint32_t pos = count + atomicAdd(&ctl.chunk_count[step % 3], c);
+        if (pos + c > L) {
+          overflow = true;
+        } else {
+          const Raw* kv = reinterpret_cast<const Raw*>(&v);
+          uint32_t w = pos;
+#pragma unroll
+          for (int i = 0; i < VK; ++i) {
+            if ((acc >> i) & 1u) {
+              list_raw[w] = kv[i];
+              list_idx[w] = i0 + (uint32_t)i;
+              ++w;
+            }
+          }
+        }
+      }
+    }
+    return overflow;
+  };
+
+  // Vectors [v0, v1) of a ring stage: offer them; if the list overflows,
+  // trim the list (as it was before the attempt) to tighten the bound and
+  // offer them again; if they overflow even a trimmed list, keep the k best
+  // of the list and all of those keys.
+  auto process_vectors = [&](const uint4* stage, uint32_t v0, uint32_t v1, uint32_t idx0) {
+    const Raw* stage_keys = reinterpret_cast<const Raw*>(stage);
+    for (;;) {
+      const bool overflow = offer_chunk(stage, v0, v1, idx0);
+      if (!__syncthreads_or(overflow)) {
+        finish_step(true);
+        return;
+      }
+      finish_step(false); // drop this attempt's appends
+      if (count > k) {
+        set_bound(trim_into<TR, NT>(ctl, list_src(list_raw, list_idx, count), list_raw, list_idx, k, dirmask,
+                                    pl, cbuf));
+      } else {
+        select_union(stage_keys + (size_t)v0 * VK, idx0 + v0 * VK, (v1 - v0) * VK);
+        return;
+      }
+    }
   };
 
   // Unaligned head / tail keys: plain loads, one per thread.
   auto offer_edge = [&](uint32_t e_begin, uint32_t e_cnt) {
+    if (count + e_cnt > L) // keep room for the edge (never happens with a list of k + 512)
+      set_bound(trim_into<TR, NT>(ctl, list_src(list_raw, list_idx, count), list_raw, list_idx, k, dirmask, pl, cbuf));
     uint4 vec[U];
     uint32_t vc[U], i0[U];
 #pragma unroll
@@ -228,8 +351,9 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
       vc[0] = 1;
       i0[0] = e_begin + threadIdx.x;
     }
-    if (__syncthreads_or(offer(vec, vc, i0)))
-      after_chunk(true);
+    offer(vec, vc, i0); // cannot overflow: count + e_cnt <= L
+    __syncthreads();
+    finish_step(true);
   };
 
   if (has_head && fwd)
@@ -245,24 +369,37 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
     const uint32_t vb = v_lo + chunk_of_step(s) * kChunkVec;
     const uint32_t nv = min(kChunkVec, v_hi - vb);
     const uint4* stage = reinterpret_cast<const uint4*>(ring + (size_t)st * kChunkBytes);
-    uint4 vec[U];
-    uint32_t vc[U], i0[U];
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const uint32_t t = (uint32_t)j * NT + threadIdx.x;
-      const bool ok = t < nv && copies_ok;
-      vec[j] = ok ? stage[t] : make_uint4(0, 0, 0, 0);
-      vc[j] = ok ? (uint32_t)VK : 0u;
-      i0[j] = head + (vb + t) * VK;
+    const Raw* stage_keys = reinterpret_cast<const Raw*>(stage);
+    const uint32_t nkeys = copies_ok ? nv * VK : 0u;
+    const uint32_t idx0 = head + vb * VK;
+    if (open) {
+      if (count + nkeys <= k) {
+        // still fewer than k keys in all: every one of them is selected so far
+        for (uint32_t e = threadIdx.x; e < nkeys; e += NT) {
+          list_raw[count + e] = stage_keys[e];
+          list_idx[count + e] = idx0 + e;
+        }
+        __syncthreads();
+        count += nkeys;
+      } else {
+        // the first bound: the k best of the list and the most preferred keys
+        // of this chunk (enough to pass k, at least kBootKeys); the rest of the
+        // chunk comes later in preference order and is offered against it
+        const uint32_t want = max(k + 1 - count, (uint32_t)kBootKeys);
+        const uint32_t nb = min(nv, (want + VK - 1) / VK);
+        const uint32_t b0 = fwd ? 0u : nv - nb; // first vector of the bootstrap part
+        select_union(stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nb * VK);
+        if (nb < nv)
+          process_vectors(stage, fwd ? nb : 0u, fwd ? nv : nv - nb, idx0);
+      }
+    } else if (copies_ok) {
+      process_vectors(stage, 0u, nv, idx0);
     }
-    const bool over = offer(vec, vc, i0);
-    const int any_over = __syncthreads_or(over); // also ends every read of this stage
+    // every read of this stage is over: refill it
     if (threadIdx.x == 0 && copies_ok && issued < nchunks) {
-      issue(issued); // refill the stage just released
+      issue(issued);
       ++issued;
     }
-    if (any_over)
-      after_chunk(true);
   }
   if (!copies_ok && threadIdx.x == 0) {
     // let every copy still in flight land before this CTA's shared memory is released
@@ -277,11 +414,8 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
 
   // local top-k of this CTA's slice
   __syncthreads();
-  uint32_t count = ctl.list_count;
-  if (count > k) {
-    trim_list<TR, NT>(ctl, list_raw, list_idx, count, k, dirmask, p.prefer_larger != 0);
-    count = k;
-  }
+  if (count > k)
+    set_bound(trim_into<TR, NT>(ctl, list_src(list_raw, list_idx, count), list_raw, list_idx, k, dirmask, pl, cbuf));
 
   Raw* out_keys = reinterpret_cast<Raw*>(p.out_keys) + seg * (int64_t)k;
   int32_t* out_values = p.out_values ? p.out_values + seg * (int64_t)k : nullptr;
@@ -334,7 +468,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
       return;
     uint32_t total = ctl.gather_count;
     if (total > k) {
-      trim_list<TR, NT>(ctl, g_raw, g_idx, total, k, dirmask, p.prefer_larger != 0);
+      trim_into<TR, NT>(ctl, list_src(g_raw, g_idx, total), g_raw, g_idx, k, dirmask, pl, cbuf);
       total = k;
     }
     unsigned char* scratch = ring + align16(cap * sizeof(Raw)) + align16(cap * 4u);
@@ -407,8 +541,9 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   const uint32_t f_total = m - ties_needed;
 
   // cross-CTA count scan in preference order
+  const Src<Raw> lsrc = list_src(list_raw, list_idx, count);
   const uint2 tot = scan_list<TR, NT>(
-    ctl, list_raw, list_idx, count, dirmask,
+    ctl, lsrc, dirmask,
     [&](uint32_t, Raw, uint32_t, Rank rk) {
       const Rank mr = rk & sel.mask;
       return mr < sel.prefix ? 1 : (mr == sel.prefix ? 2 : 0);
@@ -431,10 +566,14 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   // this CTA's share of the boundary ties, chosen by source index
   const uint32_t quota = ties_needed > tbase ? min(tot.y, ties_needed - tbase) : 0u;
   if (quota > 0 && quota < tot.y)
-    select_ties<TR, NT>(ctl, list_raw, list_idx, count, quota, dirmask, p.prefer_larger != 0, sel);
+  {
+    CandBuf cb = cbuf;
+    cb.n = ~0u;
+    select_ties<TR, NT>(ctl, lsrc, quota, dirmask, pl, sel, cb);
+  }
   const bool take_ties = quota > 0;
   auto classify = [&](uint32_t, Raw, uint32_t ki, Rank rk) {
-    const int c = sel.classify(rk, pref_index(ki, p.prefer_larger != 0));
+    const int c = sel.classify(rk, pref_index(ki, pl));
     return (c == 2 && !take_ties) ? 0 : c;
   };
   auto position = [&](int cls, uint32_t r1, uint32_t r2) {
@@ -442,7 +581,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   };
 
   if (!p.sorted) {
-    scan_list<TR, NT>(ctl, list_raw, list_idx, count, dirmask, classify,
+    scan_list<TR, NT>(ctl, lsrc, dirmask, classify,
                       [&](uint32_t, Raw kr, uint32_t ki, Rank, int cls, uint32_t r1, uint32_t r2) {
                         const uint32_t pos = position(cls, r1, r2);
                         out_keys[pos] = kr;
@@ -458,7 +597,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   unsigned char* scratch = ring + align16(m * sizeof(Raw)) + align16(m * 4u);
   const uint32_t graw = dsmem_map(smem_addr(g_raw), leader);
   const uint32_t gidx = dsmem_map(smem_addr(g_idx), leader);
-  scan_list<TR, NT>(ctl, list_raw, list_idx, count, dirmask, classify,
+  scan_list<TR, NT>(ctl, lsrc, dirmask, classify,
                     [&](uint32_t, Raw kr, uint32_t ki, Rank, int cls, uint32_t r1, uint32_t r2) {
                       const uint32_t pos = position(cls, r1, r2);
                       dsmem_st(graw + pos * (uint32_t)sizeof(Raw), kr);
