@@ -76,7 +76,7 @@ struct Plan {
   LaunchShape shape;
   uint32_t list_cap;
   uint32_t ring_bytes;
-  bool merge_gather;
+  int merge_gather;
 };
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
@@ -84,7 +84,7 @@ uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 // Candidate-list room beyond k: keys accepted after a selection before the
 // list overflows and the next selection (over the list and the chunk being
 // read) tightens the bound.
-uint32_t list_slack(uint32_t k) { return std::max(512u, k / 2); }
+uint32_t list_slack(uint32_t k) { return std::max(1024u, k / 2); }
 
 // Shared-memory sizing for a given k and cluster width. The ring doubles as
 // sort scratch and, in a cluster leader, as gather space.
@@ -95,19 +95,22 @@ Plan size_plan(const KeyOps& ops, int32_t k, int cluster)
   const uint32_t uk = (uint32_t)k;
   pl.list_cap = align_up(uk + list_slack(uk), 32);
   const uint32_t stream_ring = kStages * kChunkBytes;
-  const uint32_t sort_need = sort_scratch_bytes(uk, ops.rank_bits);
+  const uint32_t sort_need = std::max(sort_scratch_bytes(uk, ops.rank_bits), finalize_scratch_bytes(kCountMax));
   uint32_t need = sort_need;
-  pl.merge_gather = false;
+  pl.merge_gather = 0;
   if (cluster > 1) {
-    const uint32_t cap = (uint32_t)cluster * uk;
-    const uint32_t gather_need = align16(cap * kb) + align16(cap * 4u) + sort_need;
-    pl.merge_gather = gather_need <= stream_ring;
-    need = pl.merge_gather ? gather_need : align16(uk * kb) + align16(uk * 4u) + sort_need;
+    // 2: every CTA's whole list fits in the leader (no local trims);
+    // 1: every CTA's local top-k fits; 0: histogram merge through DSMEM
+    auto gather_need = [&](uint32_t cap) { return align16(cap * kb) + align16(cap * 4u) + sort_need; };
+    if (gather_need((uint32_t)cluster * uk) <= stream_ring)
+      pl.merge_gather = 1;
+    need = pl.merge_gather ? gather_need((uint32_t)cluster * (pl.merge_gather == 2 ? pl.list_cap : uk))
+                           : align16(uk * kb) + align16(uk * 4u) + sort_need;
   }
   pl.ring_bytes = align_up(std::max(stream_ring, need), 128);
   pl.shape.threads = kThreads;
   pl.shape.cluster = cluster;
-  pl.shape.smem = kCtrlBytes + pl.ring_bytes + list_bytes(pl.list_cap, kb) + kCandBytes;
+  pl.shape.smem = kCtrlBytes + pl.ring_bytes + 2 * list_bytes(pl.list_cap, kb) + kCandBytes;
   return pl;
 }
 
@@ -309,7 +312,7 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
     p.dirmask &= 0xffffffffull;
   p.k = k;
   p.list_cap = pl.list_cap;
-  p.merge_gather = pl.merge_gather ? 1 : 0;
+  p.merge_gather = pl.merge_gather;
   p.ring_stages = kStages;
   p.ring_bytes = pl.ring_bytes;
   p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;

@@ -26,6 +26,10 @@ struct Ctrl {
   uint32_t hist[2][kBuckets];     // digit histograms (double buffered; zero outside a selection)
   uint32_t hist_merged[kBuckets]; // cluster leader: histogram pushed by the other CTAs
   uint32_t res[4];                // selection result of a pass: bucket, count before, bucket count
+  uint32_t sel_and[2][2];         // selection: AND of keys seen in passes 0 / 1 (one or two words)
+  uint32_t sel_or[2][2];          // selection: OR of keys seen in passes 0 / 1
+  uint32_t sel_ncand;             // selection: candidates stored in the position buffer
+  uint32_t kept;                  // compaction: entries written so far
   uint32_t chunk_count[3];        // entries appended during a chunk (three in rotation)
   uint32_t gather_count;          // cluster leader: entries gathered from the cluster
   uint32_t front_base;            // cross-CTA scan: selected entries of preceding CTAs
@@ -57,6 +61,16 @@ __device__ __forceinline__ Src<Raw> list_src(const Raw* raw, const uint32_t* idx
 // Warp 0 of the block: find the bucket holding the krem-th best candidate.
 // `h` holds the 8 bucket counts this lane owns (buckets 8*lane .. 8*lane+7).
 // Writes bucket, count before it and its count to res[].
+__device__ __forceinline__ void find_bucket(const uint32_t (&h)[8], uint32_t krem, uint32_t* res);
+// The same, reading the lane's 8 counts from a 16-byte aligned histogram with
+// two conflict-free 16-byte loads.
+__device__ __forceinline__ void find_bucket_in(const uint32_t* hist, uint32_t krem, uint32_t* res)
+{
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 2 * lane_id();
+  const uint4 a = h4[0], b = h4[1];
+  const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  find_bucket(h, krem, res);
+}
 __device__ __forceinline__ void find_bucket(const uint32_t (&h)[8], uint32_t krem, uint32_t* res)
 {
   const uint32_t lane = lane_id();
@@ -101,21 +115,91 @@ struct CandBuf {
   uint32_t n;     // filled by radix_select: candidates stored, or ~0u if not compacted
 };
 
-// Warp-wide AND / OR of the keys of the lanes where `on` holds, folded into
-// shared words with native 32-bit atomics (one pair per warp and word).
-__device__ __forceinline__ void warp_and_or(uint32_t* a, uint32_t* o, bool on, uint32_t v)
+// Folds a thread's AND / OR of keys into the shared words (one warp
+// reduction and one native 32-bit atomic per word and warp).
+__device__ __forceinline__ void fold_and_or(uint32_t* a, uint32_t* o, uint32_t va, uint32_t vo)
 {
-  const uint32_t wa = __reduce_and_sync(kFull, on ? v : ~0u);
-  const uint32_t wo = __reduce_or_sync(kFull, on ? v : 0u);
+  va = __reduce_and_sync(kFull, va);
+  vo = __reduce_or_sync(kFull, vo);
   if (lane_id() == 0) {
-    atomicAnd(a, wa);
-    atomicOr(o, wo);
+    atomicAnd(a, va);
+    atomicOr(o, vo);
   }
 }
-__device__ __forceinline__ void warp_and_or(uint32_t* a, uint32_t* o, bool on, uint64_t v)
+__device__ __forceinline__ void fold_and_or(uint32_t* a, uint32_t* o, uint64_t va, uint64_t vo)
 {
-  warp_and_or(a, o, on, (uint32_t)v);
-  warp_and_or(a + 1, o + 1, on, (uint32_t)(v >> 32));
+  fold_and_or(a, o, (uint32_t)va, (uint32_t)vo);
+  fold_and_or(a + 1, o + 1, (uint32_t)(va >> 32), (uint32_t)(vo >> 32));
+}
+template <class Key>
+__device__ __forceinline__ Key read_word(const uint32_t* w)
+{
+  if constexpr (sizeof(Key) == 8)
+    return ((Key)w[1] << 32) | w[0];
+  else
+    return (Key)w[0];
+}
+
+// Boundary candidates left at which a selection switches to counting.
+constexpr uint32_t kFinishMax = 64;
+
+// Warp 0: the candidates (positions pos[0..npos)) whose key matches r's
+// prefix -- at most kFinishMax of them -- are gathered, and the krem-th
+// best key value v among them is found by counting. Writes v (one or two
+// words) to res[0..1], the number of candidates better than v to res[2] and
+// the number equal to v to res[3]. Uses ctl.scan_tot as staging.
+template <class Key, class Get>
+__device__ void finish_by_count(Ctrl& ctl, const uint16_t* pos, uint32_t npos, const Radix<Key>& r, Get&& get)
+{
+  Key* small = reinterpret_cast<Key*>(&ctl.scan_tot[0][0]); // 64 keys
+  const uint32_t lane = lane_id();
+  uint32_t n = 0;
+  for (uint32_t base = 0; base < npos; base += 32) {
+    const uint32_t i = base + lane;
+    Key key = 0;
+    bool on = false;
+    if (i < npos)
+      on = get((uint32_t)pos[i], key) && (key & r.mask) == r.prefix;
+    const uint32_t bal = __ballot_sync(kFull, on);
+    const uint32_t slot = n + __popc(bal & lanemask_lt());
+    if (on && slot < kFinishMax)
+      small[slot] = key;
+    n += __popc(bal);
+  }
+  __syncwarp();
+  if (n > kFinishMax)
+    n = kFinishMax; // cannot happen: the caller checked the bucket count
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t i = lane + 32u * (uint32_t)q;
+    const Key v = i < n ? small[i] : (Key)0;
+    uint32_t less = 0, eq = 0;
+    for (uint32_t j = 0; j < n; ++j) {
+      const Key w = small[j];
+      less += w < v ? 1u : 0u;
+      eq += w == v ? 1u : 0u;
+    }
+    if (i < n && less < r.krem && r.krem <= less + eq) {
+      // every lane holding this value writes the same result
+      if constexpr (sizeof(Key) == 8) {
+        ctl.res[0] = (uint32_t)v;
+        ctl.res[1] = (uint32_t)(v >> 32);
+      } else {
+        ctl.res[0] = (uint32_t)v;
+      }
+      ctl.res[2] = less;
+      ctl.res[3] = eq;
+    }
+  }
+}
+
+// Resets the selection scratch (called before a selection's first barrier by
+// thread 0 of a block that has passed a barrier since the last selection).
+__device__ __forceinline__ void reset_select_scratch(Ctrl& ctl)
+{
+  ctl.sel_ncand = 0;
+  ctl.sel_and[0][0] = ctl.sel_and[0][1] = ctl.sel_and[1][0] = ctl.sel_and[1][1] = ~0u;
+  ctl.sel_or[0][0] = ctl.sel_or[0][1] = ctl.sel_or[1][0] = ctl.sel_or[1][1] = 0u;
 }
 
 // One radix selection: among the candidates (get(e, key) returns true) of
@@ -127,106 +211,93 @@ __device__ __forceinline__ void warp_and_or(uint32_t* a, uint32_t* o, bool on, u
 // ("Implement Segmented TopK using Thread-Block-Clusters", sections 1.2
 // "Radix (digit) top-k" and 1.4 "Early stop").
 //
-// Work saving: the second pass also stores the positions of the remaining
-// candidates in `cb` (when they fit) and the AND / OR of their keys; later
-// passes then visit only those positions, and a digit on which all of them
-// agree is folded without a pass.
-// Requires at least kk candidates. Block-wide; leaves both histograms zero.
+// Work saving: pass 0 also records the AND / OR of every candidate key and
+// pass 1 those of the remaining candidates, together with their positions
+// in `cb` when they fit; later passes then visit only those positions, and a
+// digit on which all remaining candidates agree is folded without a pass.
+// Each thread takes 4 entries per loop trip, loads first.
+// Requires at least kk candidates. Block-wide; the selection scratch must be
+// reset (reset_select_scratch) and is reset again on return; both
+// histograms are zero before and after.
 template <class Key, int KEY_BITS, int NT, class Get>
 __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* dom, uint32_t dom_n,
                                    uint32_t kk, CandBuf& cb, Get&& get)
 {
   constexpr int P = KEY_BITS / kDigitBits;
+  constexpr int UNR = 4;
   Radix<Key> r{(Key)0, (Key)0, kk, false};
-  uint32_t* kand = reinterpret_cast<uint32_t*>(&ctl.red[0]); // AND of candidate keys (1 or 2 words)
-  uint32_t* kor = reinterpret_cast<uint32_t*>(&ctl.red[1]);  // OR of candidate keys
   const uint32_t span = dom ? dom_n : count;
-  uint32_t* ncand = &ctl.res[3];
+  const bool can_compact = cb.pos != nullptr;
   bool compacted = false;
-  Key diff = ~(Key)0; // digits that differ among the candidates (all, until known)
+  Key diff = ~(Key)0; // digits that may differ among the remaining candidates
   Key kand_v = 0;
-  int hb = 0; // histogram buffer of the current pass
+  int hb = 0;         // histogram buffer of the current pass
   for (int p = 0; p < P; ++p) {
     const int shift = KEY_BITS - kDigitBits * (p + 1);
     const Key dmask = (Key)(kBuckets - 1) << shift;
-    if (p >= 2 && !(diff & dmask)) {
-      // every candidate has the same digit here: fold it without a pass
+    if (p >= 1 && !(diff & dmask)) {
+      // every remaining candidate has the same digit here: fold it without a pass
       r.prefix |= kand_v & dmask;
       r.mask |= dmask;
       continue;
     }
     uint32_t* h = ctl.hist[hb];
-    const bool collect = p == 1 && cb.pos != nullptr;
-    if (compacted) {
-      const uint32_t nc = *ncand;
-      for (uint32_t i = threadIdx.x; i < nc; i += NT) {
-        Key key;
-        const uint32_t e = cb.pos[i];
-        if (get(e, key) && (key & r.mask) == r.prefix)
-          atomicAdd(&h[(uint32_t)(key >> shift) & (kBuckets - 1)], 1u);
-      }
-    } else if (!collect) {
-      for (uint32_t i = threadIdx.x; i < span; i += NT) {
-        Key key;
-        const uint32_t e = dom ? dom[i] : i;
-        if (get(e, key) && (key & r.mask) == r.prefix)
-          atomicAdd(&h[(uint32_t)(key >> shift) & (kBuckets - 1)], 1u);
-      }
-    } else {
-      // uniform trip count: the warp-wide ballots and reductions need every lane
-      for (uint32_t base = 0; base < span; base += NT) {
-        const uint32_t i = base + threadIdx.x;
-        Key key = 0;
-        uint32_t e = 0;
-        bool on = false;
-        if (i < span) {
-          e = dom ? dom[i] : i;
-          on = get(e, key) && (key & r.mask) == r.prefix;
+    const bool rec = p <= 1; // record AND / OR
+    const bool collect = p == 1 && can_compact;
+    const uint32_t n_visit = compacted ? ctl.sel_ncand : span;
+    Key ta = ~(Key)0, to = (Key)0;
+    for (uint32_t base = 0; base < n_visit; base += NT * UNR) {
+      Key key[UNR];
+      uint32_t e[UNR];
+      bool on[UNR];
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        const uint32_t i = base + (uint32_t)u * NT + threadIdx.x;
+        on[u] = false;
+        key[u] = 0;
+        e[u] = 0;
+        if (i < n_visit) {
+          e[u] = compacted ? (uint32_t)cb.pos[i] : (dom ? (uint32_t)dom[i] : i);
+          on[u] = get(e[u], key[u]) && (key[u] & r.mask) == r.prefix;
         }
-        if (on)
-          atomicAdd(&h[(uint32_t)(key >> shift) & (kBuckets - 1)], 1u);
-        const uint32_t bal = __ballot_sync(kFull, on);
-        if (bal) {
-          uint32_t slot = 0;
-          if (lane_id() == 0)
-            slot = atomicAdd(ncand, __popc(bal));
-          slot = __shfl_sync(kFull, slot, 0) + __popc(bal & lanemask_lt());
-          if (on && slot < cb.cap)
-            cb.pos[slot] = (uint16_t)e;
-          warp_and_or(kand, kor, on, key);
+      }
+      uint32_t nc = 0;
+#pragma unroll
+      for (int u = 0; u < UNR; ++u) {
+        if (on[u]) {
+          atomicAdd(&h[(uint32_t)(key[u] >> shift) & (kBuckets - 1)], 1u);
+          ta &= key[u];
+          to |= key[u];
+          ++nc;
+        }
+      }
+      if (collect && nc) {
+        uint32_t slot = atomicAdd(&ctl.sel_ncand, nc);
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+          if (on[u]) {
+            if (slot < cb.cap)
+              cb.pos[slot] = (uint16_t)e[u];
+            ++slot;
+          }
         }
       }
     }
+    if (rec)
+      fold_and_or(ctl.sel_and[p], ctl.sel_or[p], ta, to);
     if (threadIdx.x < kBuckets)
       ctl.hist[hb ^ 1][threadIdx.x] = 0;
-    if (threadIdx.x == 0 && p == 0 && cb.pos != nullptr) {
-      *ncand = 0;
-      kand[0] = kand[1] = ~0u;
-      kor[0] = kor[1] = 0u;
-    }
     __syncthreads();
-    if (threadIdx.x < 32) {
-      uint32_t hh[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        hh[i] = h[8 * threadIdx.x + i];
-      find_bucket(hh, r.krem, ctl.res);
-    }
+    if (threadIdx.x < 32)
+      find_bucket_in(h, r.krem, ctl.res);
     __syncthreads();
     const uint32_t b = ctl.res[0], before = ctl.res[1], cnt = ctl.res[2];
-    if (collect) {
-      compacted = *ncand <= cb.cap;
-      Key a, o;
-      if constexpr (sizeof(Key) == 8) {
-        a = ((Key)kand[1] << 32) | kand[0];
-        o = ((Key)kor[1] << 32) | kor[0];
-      } else {
-        a = (Key)kand[0];
-        o = (Key)kor[0];
-      }
-      kand_v = a;
-      diff = a ^ o;
+    if (rec) {
+      kand_v = read_word<Key>(ctl.sel_and[p]);
+      diff = kand_v ^ read_word<Key>(ctl.sel_or[p]);
     }
+    if (collect)
+      compacted = ctl.sel_ncand <= cb.cap;
     r.krem -= before;
     r.prefix |= (Key)b << shift;
     r.mask |= dmask;
@@ -237,10 +308,25 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* do
       r.stopped = true;
       break;
     }
-    // ctl.res, the candidate count and h are rewritten only after the next barrier
+    if (compacted && cnt <= kFinishMax && p + 1 < P) {
+      // few candidates left: resolve the boundary key by counting (warp 0)
+      __syncthreads(); // everyone has read ctl.res
+      if (threadIdx.x < 32)
+        finish_by_count<Key>(ctl, cb.pos, ctl.sel_ncand, r, get);
+      __syncthreads();
+      r.prefix = read_word<Key>(ctl.res);
+      r.mask = ~(Key)0;
+      r.krem -= ctl.res[2];
+      r.stopped = ctl.res[3] == r.krem;
+      break;
+    }
+    // ctl.res and h are rewritten only after the next barrier
   }
-  cb.n = compacted ? *ncand : ~0u;
-  __syncthreads(); // histograms zero and ctl.res / ctl.red free for the next selection
+  cb.n = compacted ? ctl.sel_ncand : ~0u;
+  __syncthreads(); // everyone has read the scratch
+  if (threadIdx.x == 0)
+    reset_select_scratch(ctl);
+  __syncthreads(); // histograms zero and scratch reset for the next selection
   return r;
 }
 
@@ -401,10 +487,10 @@ __device__ __forceinline__ Rank block_max(Ctrl& ctl, Rank v)
 }
 
 // Keep the kk best entries of `src` (size > kk > 0), written to dst[0, kk)
-// in their order in src. dst may be src's list arrays: every entry is written
-// at or before its own position, after its tile has been read. Returns the
-// largest rank kept: later keys (which come after every kept one in
-// preference order) are accepted only below it.
+// in no particular order (warp-aggregated atomic positions, one pass, no
+// scan). dst must not overlap src's arrays. Returns the largest rank kept:
+// later keys (which come after every kept one in preference order) are
+// accepted only below it.
 template <class TR, int NT>
 __device__ __noinline__ typename TR::Rank trim_into(Ctrl& ctl, const Src<typename TR::Raw> src,
                                                     typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t kk,
@@ -413,17 +499,37 @@ __device__ __noinline__ typename TR::Rank trim_into(Ctrl& ctl, const Src<typenam
   using Raw = typename TR::Raw;
   using Rank = typename TR::Rank;
   const Selection<Rank> s = block_select<TR, NT>(ctl, src, kk, dirmask, prefer_larger, cb);
+  if (threadIdx.x == 0)
+    ctl.kept = 0;
+  __syncthreads();
   Rank mx = 0;
-  scan_list<TR, NT>(
-    ctl, src, dirmask,
-    [&](uint32_t, Raw, uint32_t ki, Rank rk) { return s.classify(rk, pref_index(ki, prefer_larger)); },
-    [&](uint32_t, Raw kr, uint32_t ki, Rank rk, int, uint32_t r1, uint32_t r2) {
-      const uint32_t pos = r1 + r2;
-      dst_raw[pos] = kr;
-      dst_idx[pos] = ki;
-      mx = rk > mx ? rk : mx;
-    });
-  return block_max<Rank, NT>(ctl, mx);
+  const uint32_t n = src.size();
+  for (uint32_t base = 0; base < n; base += NT) {
+    const uint32_t e = base + threadIdx.x;
+    bool keep = false;
+    Raw kr = 0;
+    uint32_t ki = 0;
+    Rank rk = 0;
+    if (e < n) {
+      kr = src.key(e);
+      ki = src.index(e);
+      rk = TR::rank(kr, dirmask);
+      keep = s.classify(rk, pref_index(ki, prefer_larger)) != 0;
+    }
+    const uint32_t bal = __ballot_sync(kFull, keep);
+    if (bal) {
+      uint32_t wb = 0;
+      if (lane_id() == 0)
+        wb = atomicAdd(&ctl.kept, __popc(bal));
+      const uint32_t pos = __shfl_sync(kFull, wb, 0) + __popc(bal & lanemask_lt());
+      if (keep && pos < kk) { // pos < kk always holds for a valid selection; guards dst
+        dst_raw[pos] = kr;
+        dst_idx[pos] = ki;
+        mx = rk > mx ? rk : mx;
+      }
+    }
+  }
+  return block_max<Rank, NT>(ctl, mx); // its barriers also publish dst
 }
 
 // ---------------------------------------------------------------------------
@@ -492,6 +598,116 @@ __host__ __device__ inline uint32_t sort_scratch_bytes(uint32_t m, int rank_bits
 {
   const uint32_t n2 = next_pow2(m < 2 ? 2 : m);
   return rank_bits > 32 ? n2 * 16u : n2 * 12u;
+}
+
+// ---------------------------------------------------------------------------
+// Selection and ordering by counting, for small sets (n <= kCountMax): every
+// entry's position is the number of entries with a smaller key, keys being
+// unique composites. Costs n^2 / NT compares per thread and two barriers,
+// far below the fixed cost of digit passes on a few hundred entries.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kCountMax = 128;
+
+// pos[i] = #{ j < n : key_j < key_i } for unique keys (hi[i], lo[i]) (lo may
+// be null for 64-bit keys). Every thread handles up to EC entries.
+template <int NT, int EC>
+__device__ __forceinline__ void count_ranks(const uint64_t* hi, const uint64_t* lo, uint32_t n, uint32_t* pos)
+{
+  uint64_t mh[EC], ml[EC];
+  uint32_t c[EC];
+#pragma unroll
+  for (int q = 0; q < EC; ++q) {
+    const uint32_t i = threadIdx.x + (uint32_t)q * NT;
+    mh[q] = i < n ? hi[i] : ~0ull;
+    ml[q] = (lo && i < n) ? lo[i] : ~0ull;
+    c[q] = 0;
+  }
+  if (lo) {
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint64_t h = hi[j], l = lo[j];
+#pragma unroll
+      for (int q = 0; q < EC; ++q)
+        c[q] += (h < mh[q] || (h == mh[q] && l < ml[q])) ? 1u : 0u;
+    }
+  } else {
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint64_t h = hi[j];
+#pragma unroll
+      for (int q = 0; q < EC; ++q)
+        c[q] += h < mh[q] ? 1u : 0u;
+    }
+  }
+#pragma unroll
+  for (int q = 0; q < EC; ++q) {
+    const uint32_t i = threadIdx.x + (uint32_t)q * NT;
+    if (i < n)
+      pos[i] = c[q];
+  }
+}
+
+// Bytes of scratch finalize_small needs for n entries.
+__host__ __device__ inline uint32_t finalize_scratch_bytes(uint32_t n) { return n * (8u + 8u + 4u); }
+
+// The k best of n <= kCountMax list entries, written to one segment's output
+// slots: unsorted in selection-rank order, or stable sorted by (key, source
+// index). `scratch` holds finalize_scratch_bytes(n) bytes (shared memory);
+// the entries must be visible to the whole block.
+template <class TR, int NT>
+__device__ __noinline__ void finalize_small(const typename TR::Raw* raw, const uint32_t* idx, uint32_t n, uint32_t k,
+                                            typename TR::Rank dirmask, bool prefer_larger, bool sorted,
+                                            unsigned char* scratch, typename TR::Raw* out_keys, int32_t* out_values,
+                                            const int32_t* values)
+{
+  constexpr int EC = (int)((kCountMax + NT - 1) / NT);
+  constexpr bool wide = TR::kRankBits > 32;
+  uint64_t* kh = reinterpret_cast<uint64_t*>(scratch);
+  uint64_t* kl = kh + n;
+  uint32_t* pos = reinterpret_cast<uint32_t*>(kl + n);
+  const uint32_t m = k < n ? k : n;
+  // selection order: (rank, preference index)
+  for (uint32_t i = threadIdx.x; i < n; i += NT) {
+    const uint64_t r = (uint64_t)TR::rank(raw[i], dirmask);
+    const uint32_t pi = pref_index(idx[i], prefer_larger);
+    kh[i] = wide ? r : ((r << 32) | pi);
+    kl[i] = pi;
+  }
+  __syncthreads();
+  if (m < n) {
+    count_ranks<NT, EC>(kh, wide ? kl : nullptr, n, pos);
+    __syncthreads();
+  } else {
+    for (uint32_t i = threadIdx.x; i < n; i += NT)
+      pos[i] = i; // every entry is selected
+    __syncthreads();
+  }
+  if (!sorted) {
+    for (uint32_t i = threadIdx.x; i < n; i += NT) {
+      const uint32_t p = pos[i];
+      if (p < m) {
+        out_keys[p] = raw[i];
+        if (out_values)
+          out_values[p] = values[idx[i]];
+      }
+    }
+    return;
+  }
+  // output order among the selected: (rank, source index); the others sort last
+  for (uint32_t i = threadIdx.x; i < n; i += NT) {
+    const bool sel = pos[i] < m;
+    const uint64_t r = (uint64_t)TR::rank(raw[i], dirmask);
+    kh[i] = !sel ? ~0ull : (wide ? r : ((r << 32) | idx[i]));
+    kl[i] = !sel ? ~0ull : (uint64_t)idx[i];
+  }
+  __syncthreads();
+  count_ranks<NT, EC>(kh, wide ? kl : nullptr, n, pos);
+  for (uint32_t i = threadIdx.x; i < n; i += NT) {
+    const uint32_t p = pos[i];
+    if (p < m) {
+      out_keys[p] = raw[i];
+      if (out_values)
+        out_values[p] = values[idx[i]];
+    }
+  }
 }
 
 // Sort the m items (raw[i], idx[i]) (i < m) and write them to the output

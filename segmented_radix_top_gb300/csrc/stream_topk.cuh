@@ -51,7 +51,7 @@ struct KernelParams {
   uint32_t ring_bytes;   // ring region bytes (also sort / gather scratch)
   int32_t prefer_larger; // tie preference: larger source index first
   int32_t sorted;        // write the selected items in stable sorted order
-  int32_t merge_gather;  // cluster merge by gathering every CTA's list into the leader
+  int32_t merge_gather;  // cluster merge: 2 gather whole lists, 1 gather local top-k, 0 histograms
   int32_t flag_overlong; // report segments longer than n_hi
 };
 
@@ -64,7 +64,7 @@ __host__ __device__ inline uint32_t list_bytes(uint32_t cap, uint32_t key_bytes)
 // Keys of the first chunk used to form the first bound.
 constexpr uint32_t kBootKeys = 2048;
 // Candidate positions kept by a selection between its passes.
-constexpr uint32_t kCandCap = 8192;
+constexpr uint32_t kCandCap = 4096;
 constexpr uint32_t kCandBytes = kCandCap * 2u;
 
 template <KeyKind KK, int NT>
@@ -82,9 +82,14 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   extern __shared__ __align__(128) unsigned char smem[];
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem);
   unsigned char* ring = smem + kCtrlBytes;
-  Raw* list_raw = reinterpret_cast<Raw*>(ring + p.ring_bytes);
-  uint32_t* list_idx = reinterpret_cast<uint32_t*>(ring + p.ring_bytes + align16(p.list_cap * sizeof(Raw)));
-  uint16_t* cand_pos = reinterpret_cast<uint16_t*>(ring + p.ring_bytes + list_bytes(p.list_cap, sizeof(Raw)));
+  // two candidate-list buffers: a trim writes the kept entries into the spare one
+  unsigned char* lists = ring + p.ring_bytes;
+  const uint32_t lbytes = list_bytes(p.list_cap, sizeof(Raw));
+  Raw* list_raw = reinterpret_cast<Raw*>(lists);
+  uint32_t* list_idx = reinterpret_cast<uint32_t*>(lists + align16(p.list_cap * sizeof(Raw)));
+  Raw* spare_raw = reinterpret_cast<Raw*>(lists + lbytes);
+  uint32_t* spare_idx = reinterpret_cast<uint32_t*>(lists + lbytes + align16(p.list_cap * sizeof(Raw)));
+  uint16_t* cand_pos = reinterpret_cast<uint16_t*>(lists + 2 * lbytes);
   const CandBuf cbuf{cand_pos, kCandCap, 0u};
 
   const uint32_t C = cluster_nctarank();
@@ -118,6 +123,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   }
   if (threadIdx.x == 0) {
     ctl.chunk_count[0] = ctl.chunk_count[1] = ctl.chunk_count[2] = 0;
+    reset_select_scratch(ctl);
     ctl.gather_count = 0;
     ctl.front_base = 0;
     ctl.tie_base = 0;
@@ -169,11 +175,20 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
     open = false;
     count = k;
   };
-  // Keep the k best of the list and `n_ext` keys at `ext` (indices idx0..).
+  // Keep the k best of the list and `n_ext` keys at `ext` (indices idx0..)
+  // in the spare buffer, which becomes the list.
   auto select_union = [&](const Raw* ext, uint32_t idx0, uint32_t n_ext) {
-    set_bound(trim_into<TR, NT>(ctl, Src<Raw>{list_raw, list_idx, count, ext, idx0, n_ext}, list_raw, list_idx, k,
-                                dirmask, pl, cbuf));
+    const Rank tau = trim_into<TR, NT>(ctl, Src<Raw>{list_raw, list_idx, count, ext, idx0, n_ext}, spare_raw,
+                                       spare_idx, k, dirmask, pl, cbuf);
+    Raw* tr = list_raw;
+    list_raw = spare_raw;
+    spare_raw = tr;
+    uint32_t* ti = list_idx;
+    list_idx = spare_idx;
+    spare_idx = ti;
+    set_bound(tau);
   };
+  auto trim_list = [&]() { select_union(nullptr, 0u, 0u); };
 
   // Offer this thread's U vectors (vector j: vc[j] keys from slot 0, source
   // indices i0[j] + slot). Keys that may beat the bound are tested exactly;
@@ -325,8 +340,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
       }
       finish_step(false); // drop this attempt's appends
       if (count > k) {
-        set_bound(trim_into<TR, NT>(ctl, list_src(list_raw, list_idx, count), list_raw, list_idx, k, dirmask,
-                                    pl, cbuf));
+        trim_list();
       } else {
         select_union(stage_keys + (size_t)v0 * VK, idx0 + v0 * VK, (v1 - v0) * VK);
         return;
@@ -337,7 +351,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   // Unaligned head / tail keys: plain loads, one per thread.
   auto offer_edge = [&](uint32_t e_begin, uint32_t e_cnt) {
     if (count + e_cnt > L) // keep room for the edge (never happens with a list of k + 512)
-      set_bound(trim_into<TR, NT>(ctl, list_src(list_raw, list_idx, count), list_raw, list_idx, k, dirmask, pl, cbuf));
+      trim_list();
     uint4 vec[U];
     uint32_t vc[U], i0[U];
 #pragma unroll
@@ -412,26 +426,47 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   if (has_head && !fwd)
     offer_edge(0, head);
 
-  // local top-k of this CTA's slice
+  // local top-k of this CTA's slice, for clusters that gather top-k lists
+  // or merge histograms (a lone CTA, or a cluster that gathers whole lists,
+  // selects once when writing the output)
   __syncthreads();
-  if (count > k)
-    set_bound(trim_into<TR, NT>(ctl, list_src(list_raw, list_idx, count), list_raw, list_idx, k, dirmask, pl, cbuf));
+  if (count > k && C > 1 && p.merge_gather != 2)
+    trim_list();
 
   Raw* out_keys = reinterpret_cast<Raw*>(p.out_keys) + seg * (int64_t)k;
   int32_t* out_values = p.out_values ? p.out_values + seg * (int64_t)k : nullptr;
   const int32_t* values = p.values ? p.values + g0 : nullptr;
 
-  if (C == 1) {
-    // count == m: the list is the answer
-    if (p.sorted) {
-      sort_and_write<TR, NT>(list_raw, list_idx, count, dirmask, ring, out_keys, out_values, values);
-    } else {
-      for (uint32_t e = threadIdx.x; e < count; e += NT) {
-        out_keys[e] = list_raw[e];
-        if (out_values)
-          out_values[e] = values[list_idx[e]];
-      }
+  // The k best of n list entries (any order), written to this segment's
+  // output slots: small sets by counting, larger ones by a radix selection
+  // and then a sort of the k survivors when the output is sorted.
+  auto finish = [&](Raw* raw, uint32_t* idx, uint32_t nn, Raw* sp_raw, uint32_t* sp_idx, unsigned char* scratch) {
+    if (nn <= kCountMax) {
+      finalize_small<TR, NT>(raw, idx, nn, k, dirmask, pl, p.sorted != 0, scratch, out_keys, out_values, values);
+      return;
     }
+    uint32_t mm = nn; // every entry is selected when nn <= k
+    if (nn > k) {
+      trim_into<TR, NT>(ctl, list_src(raw, idx, nn), sp_raw, sp_idx, k, dirmask, pl, cbuf);
+      raw = sp_raw;
+      idx = sp_idx;
+      mm = k;
+    }
+    if (!p.sorted) {
+      for (uint32_t e = threadIdx.x; e < mm; e += NT) {
+        out_keys[e] = raw[e];
+        if (out_values)
+          out_values[e] = values[idx[e]];
+      }
+    } else if (mm <= kCountMax) {
+      finalize_small<TR, NT>(raw, idx, mm, mm, dirmask, pl, true, scratch, out_keys, out_values, values);
+    } else {
+      sort_and_write<TR, NT>(raw, idx, mm, dirmask, scratch, out_keys, out_values, values);
+    }
+  };
+
+  if (C == 1) {
+    finish(list_raw, list_idx, count, spare_raw, spare_idx, ring);
     return;
   }
 
@@ -441,7 +476,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
 
   if (p.merge_gather) {
     // every CTA's list (<= k entries) into the leader's ring, one warp-wide atomic per 32 entries
-    const uint32_t cap = C * k;
+    const uint32_t cap = C * (p.merge_gather == 2 ? L : k);
     Raw* g_raw = reinterpret_cast<Raw*>(ring);
     uint32_t* g_idx = reinterpret_cast<uint32_t*>(ring + align16(cap * sizeof(Raw)));
     const uint32_t graw = dsmem_map(smem_addr(g_raw), leader);
@@ -466,21 +501,8 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
     cluster_sync(); // the leader holds every candidate
     if (rank != leader)
       return;
-    uint32_t total = ctl.gather_count;
-    if (total > k) {
-      trim_into<TR, NT>(ctl, list_src(g_raw, g_idx, total), g_raw, g_idx, k, dirmask, pl, cbuf);
-      total = k;
-    }
     unsigned char* scratch = ring + align16(cap * sizeof(Raw)) + align16(cap * 4u);
-    if (p.sorted) {
-      sort_and_write<TR, NT>(g_raw, g_idx, total, dirmask, scratch, out_keys, out_values, values);
-    } else {
-      for (uint32_t e = threadIdx.x; e < total; e += NT) {
-        out_keys[e] = g_raw[e];
-        if (out_values)
-          out_values[e] = values[g_idx[e]];
-      }
-    }
+    finish(g_raw, g_idx, ctl.gather_count, list_raw, list_idx, scratch); // the leader's own lists are free now
     return;
   }
 
