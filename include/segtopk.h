@@ -82,9 +82,7 @@ typedef enum {
 } segtopk_status;
 
 /* Largest k this build serves (the selected items of one segment are held
- * and sorted on chip). Calls with a larger k return SEGTOPK_ERROR_NOT_SUPPORTED
- * unless every segment is no longer than k and the ordering is UNSORTED
- * (then every key is selected and the call is a copy). */
+ * and sorted on chip). Calls with a larger k return SEGTOPK_ERROR_NOT_SUPPORTED. */
 #define SEGTOPK_MAX_K 2048
 
 /* Largest segment length (keys) accepted: segment-local indices are 32-bit. */

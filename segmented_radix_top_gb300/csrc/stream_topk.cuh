@@ -6,7 +6,7 @@
 // ties, ties taken in source-index order.
 //
 // GB300 design (what differs from the pages' CUB kernel):
-//  * Keys stream once from HBM through a ring of 16 KiB shared-memory stages
+//  * Keys stream once from HBM through a ring of 32 KiB shared-memory stages
 //    filled by 1-D bulk copies (TMA), one mbarrier per stage, chunks visited
 //    in preference order (descending source index for prefer_larger_index).
 //  * Instead of keeping the whole segment resident and re-reading it every

@@ -1,5 +1,5 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle,
-bit-exact, on seeded inputs that span several 16 KiB chunks, ragged tails,
+bit-exact, on seeded inputs that span several 32 KiB chunks, ragged tails,
 unaligned segment starts, single CTAs and forced thread-block clusters."""
 import itertools
 
