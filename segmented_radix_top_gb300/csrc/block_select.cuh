@@ -104,7 +104,8 @@ struct Radix {
   Key prefix;      // resolved leading digits of the boundary key
   Key mask;        // which digits are resolved
   uint32_t krem;   // how many boundary candidates are still needed
-  bool stopped;    // the boundary bucket held exactly krem candidates
+  uint32_t cnt;    // candidates in the boundary bucket
+  bool stopped;    // the whole boundary bucket may be taken (cnt - krem <= slack)
 };
 
 // Candidate-position buffer (shared memory) that a selection may use to
@@ -209,7 +210,13 @@ __device__ __forceinline__ void reset_select_scratch(Ctrl& ctl)
 // finds the bucket holding the krem-th best, narrows krem and folds the digit
 // into the prefix; it stops when that bucket holds exactly krem candidates
 // ("Implement Segmented TopK using Thread-Block-Clusters", sections 1.2
-// "Radix (digit) top-k" and 1.4 "Early stop").
+// "Radix (digit) top-k" and 1.4 "Early stop"). With slack > 0 it also stops
+// once the bucket holds at most krem + slack candidates: taking the whole
+// bucket then keeps between kk and kk + slack candidates, all of them at
+// least as good as every candidate left out. A pass after the first that
+// leaves more than abort_cnt candidates in the boundary bucket ends the
+// selection unresolved (stopped = false), for callers that only want a
+// cheap answer.
 //
 // Work saving: pass 0 also records the AND / OR of every candidate key and
 // pass 1 those of the remaining candidates, together with their positions
@@ -221,11 +228,11 @@ __device__ __forceinline__ void reset_select_scratch(Ctrl& ctl)
 // histograms are zero before and after.
 template <class Key, int KEY_BITS, int NT, class Get>
 __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* dom, uint32_t dom_n,
-                                   uint32_t kk, CandBuf& cb, Get&& get)
+                                   uint32_t kk, uint32_t slack, uint32_t abort_cnt, CandBuf& cb, Get&& get)
 {
   constexpr int P = KEY_BITS / kDigitBits;
   constexpr int UNR = 4;
-  Radix<Key> r{(Key)0, (Key)0, kk, false};
+  Radix<Key> r{(Key)0, (Key)0, kk, 0u, false};
   const uint32_t span = dom ? dom_n : count;
   const bool can_compact = cb.pos != nullptr;
   bool compacted = false;
@@ -299,15 +306,18 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* do
     if (collect)
       compacted = ctl.sel_ncand <= cb.cap;
     r.krem -= before;
+    r.cnt = cnt;
     r.prefix |= (Key)b << shift;
     r.mask |= dmask;
     if (threadIdx.x < kBuckets)
       h[threadIdx.x] = 0; // warp 0 read it before the barrier above
     hb ^= 1;
-    if (cnt == r.krem) {
+    if (cnt - r.krem <= slack) {
       r.stopped = true;
       break;
     }
+    if (p >= 1 && cnt > abort_cnt)
+      break;
     if (compacted && cnt <= kFinishMax && p + 1 < P) {
       // few candidates left: resolve the boundary key by counting (warp 0)
       __syncthreads(); // everyone has read ctl.res
@@ -317,7 +327,8 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* do
       r.prefix = read_word<Key>(ctl.res);
       r.mask = ~(Key)0;
       r.krem -= ctl.res[2];
-      r.stopped = ctl.res[3] == r.krem;
+      r.cnt = ctl.res[3];
+      r.stopped = r.cnt - r.krem <= slack;
       break;
     }
     // ctl.res and h are rewritten only after the next barrier
@@ -369,7 +380,7 @@ __device__ void select_ties(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_
   const bool use = cb.pos != nullptr && cb.n != ~0u;
   CandBuf none{nullptr, 0u, ~0u};
   const Radix<uint32_t> ri = radix_select<uint32_t, 32, NT>(
-    ctl, src.size(), use ? cb.pos : nullptr, use ? cb.n : 0u, q, use ? none : cb, [&](uint32_t e, uint32_t& key) {
+    ctl, src.size(), use ? cb.pos : nullptr, use ? cb.n : 0u, q, 0u, ~0u, use ? none : cb, [&](uint32_t e, uint32_t& key) {
       key = pref_index(src.index(e), prefer_larger);
       return (TR::rank(src.key(e), dirmask) & mask) == prefix;
     });
@@ -377,15 +388,17 @@ __device__ void select_ties(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_
   s.imask = ri.mask;
 }
 
-// The kk best of the entries of `src` (size > kk > 0) in one CTA: a radix
-// selection on the rank code, then, if more boundary entries tie than are
-// needed, one on the preference index.
+// The kk best of the entries of `src` (size > kk > 0) in one CTA -- or,
+// with slack > 0, between kk and kk + slack entries that include them: a
+// radix selection on the rank code, then, if more boundary entries tie than
+// are needed, one on the preference index.
 template <class TR, int NT>
 __device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_t kk,
-                                                     typename TR::Rank dirmask, bool prefer_larger, CandBuf cb)
+                                                     uint32_t slack, typename TR::Rank dirmask, bool prefer_larger,
+                                                     CandBuf cb)
 {
   using Rank = typename TR::Rank;
-  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, src.size(), nullptr, 0u, kk, cb,
+  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, src.size(), nullptr, 0u, kk, slack, ~0u, cb,
                                                                [&](uint32_t e, Rank& key) {
                                                                  key = TR::rank(src.key(e), dirmask);
                                                                  return true;
@@ -486,19 +499,25 @@ __device__ __forceinline__ Rank block_max(Ctrl& ctl, Rank v)
   return m;
 }
 
-// Keep the kk best entries of `src` (size > kk > 0), written to dst[0, kk)
-// in no particular order (warp-aggregated atomic positions, one pass, no
-// scan). dst must not overlap src's arrays. Returns the largest rank kept:
-// later keys (which come after every kept one in preference order) are
-// accepted only below it.
+// Entries kept by a compaction: their number and their largest rank.
+template <class Rank>
+struct Kept {
+  Rank max_rank;
+  uint32_t n;
+};
+
+// Writes the entries of `src` that `s` selects to dst[0, cap) in no
+// particular order (warp-aggregated atomic positions, one pass, no scan).
+// dst must not overlap src's arrays. Block-wide.
 template <class TR, int NT>
-__device__ __noinline__ typename TR::Rank trim_into(Ctrl& ctl, const Src<typename TR::Raw> src,
-                                                    typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t kk,
-                                                    typename TR::Rank dirmask, bool prefer_larger, CandBuf cb)
+__device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, const Src<typename TR::Raw>& src,
+                                                               const Selection<typename TR::Rank>& s,
+                                                               typename TR::Raw* dst_raw, uint32_t* dst_idx,
+                                                               uint32_t cap, typename TR::Rank dirmask,
+                                                               bool prefer_larger)
 {
   using Raw = typename TR::Raw;
   using Rank = typename TR::Rank;
-  const Selection<Rank> s = block_select<TR, NT>(ctl, src, kk, dirmask, prefer_larger, cb);
   if (threadIdx.x == 0)
     ctl.kept = 0;
   __syncthreads();
@@ -522,14 +541,68 @@ __device__ __noinline__ typename TR::Rank trim_into(Ctrl& ctl, const Src<typenam
       if (lane_id() == 0)
         wb = atomicAdd(&ctl.kept, __popc(bal));
       const uint32_t pos = __shfl_sync(kFull, wb, 0) + __popc(bal & lanemask_lt());
-      if (keep && pos < kk) { // pos < kk always holds for a valid selection; guards dst
+      if (keep && pos < cap) { // pos < cap always holds for a valid selection; guards dst
         dst_raw[pos] = kr;
         dst_idx[pos] = ki;
         mx = rk > mx ? rk : mx;
       }
     }
   }
-  return block_max<Rank, NT>(ctl, mx); // its barriers also publish dst
+  const Rank bm = block_max<Rank, NT>(ctl, mx); // its barriers also publish dst and ctl.kept
+  const uint32_t kept = ctl.kept;
+  return Kept<Rank>{bm, kept < cap ? kept : cap};
+}
+
+// Keep the kk best entries of `src` (size > kk > 0) -- with slack > 0,
+// between kk and kk + slack entries that include them -- in dst, which holds
+// kk + slack entries. Returns the number kept and their largest rank: later
+// keys (which come after every kept one in preference order) are accepted
+// only below it.
+template <class TR, int NT>
+__device__ __noinline__ Kept<typename TR::Rank> trim_into(Ctrl& ctl, const Src<typename TR::Raw> src,
+                                                          typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t kk,
+                                                          uint32_t slack, typename TR::Rank dirmask,
+                                                          bool prefer_larger, CandBuf cb)
+{
+  const Selection<typename TR::Rank> s = block_select<TR, NT>(ctl, src, kk, slack, dirmask, prefer_larger, cb);
+  return select_into<TR, NT>(ctl, src, s, dst_raw, dst_idx, kk + slack, dirmask, prefer_larger);
+}
+
+// A speculative first bound from a sample of a slice: the smallest rank
+// edge with at least mm sample entries at or below it (mm is below the
+// number the slice needs), found by a digit selection that may stop early
+// with up to 2 mm entries. Every sample entry with rank <= edge is written
+// to dst (capacity cap); the caller then accepts later keys with rank <=
+// edge only, and must verify at the end that the slice produced enough
+// entries. Fails (ok = false, nothing written) when the entries at the
+// boundary rank are too many (heavy ties: given up as soon as a digit pass
+// after the first leaves more than 8 mm + 64 of them) or edge is the worst
+// rank.
+template <class Rank>
+struct Spec {
+  bool ok;
+  Rank edge;
+  uint32_t n;
+};
+template <class TR, int NT>
+__device__ __noinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, const Src<typename TR::Raw> src,
+                                                          typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t mm,
+                                                          uint32_t cap, typename TR::Rank dirmask, CandBuf cb)
+{
+  using Rank = typename TR::Rank;
+  constexpr Rank kWorst = (TR::kRankBits == 64) ? ~(Rank)0 : (Rank)(((uint64_t)1 << TR::kRankBits) - 1);
+  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, src.size(), nullptr, 0u, mm, mm, 8u * mm + 64u, cb,
+                                                               [&](uint32_t e, Rank& key) {
+                                                                 key = TR::rank(src.key(e), dirmask);
+                                                                 return true;
+                                                               });
+  const Rank edge = rr.prefix | (~rr.mask & kWorst);
+  const uint32_t total = mm - rr.krem + rr.cnt;
+  if (!rr.stopped || edge == kWorst || total > cap)
+    return Spec<Rank>{false, (Rank)0, 0u};
+  const Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u}; // the whole boundary bucket
+  const Kept<Rank> kp = select_into<TR, NT>(ctl, src, s, dst_raw, dst_idx, cap, dirmask, false);
+  return Spec<Rank>{true, edge, kp.n};
 }
 
 // ---------------------------------------------------------------------------

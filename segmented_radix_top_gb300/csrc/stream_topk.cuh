@@ -148,47 +148,41 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   const bool has_tail = rank == C - 1 && tail > 0;
 
   auto chunk_of_step = [&](uint32_t s) { return fwd ? s : nchunks - 1 - s; };
-  auto issue = [&](uint32_t s) {
-    const uint32_t v0 = v_lo + chunk_of_step(s) * kChunkVec;
-    const uint32_t nv = min(kChunkVec, v_hi - v0);
-    const uint32_t st = s % S;
-    mbar_arrive_expect_tx(&ctl.bars[st], nv * 16u);
-    bulk_load(ring + (size_t)st * kChunkBytes, seg_keys + head + (size_t)v0 * VK, nv * 16u, &ctl.bars[st]);
-  };
-  uint32_t issued = 0;
-  if (threadIdx.x == 0) {
-    for (; issued < S && issued < nchunks; ++issued)
-      issue(issued);
-  }
-
   // ---- streaming selection state (uniform across the block) ----
   const uint32_t L = p.list_cap;
+  const uint32_t n_slice = nvec * VK + (has_head ? head : 0u) + (has_tail ? tail : 0u);
+  // a trim may keep up to this many entries beyond k (fewer digit passes)
+  const uint32_t trim_slack = min((L - k) / 4u, max(k / 2u, 16u));
   uint32_t count = 0; // list entries
   bool open = true;   // no bound yet: every key is accepted
   Bound<Raw, Rank> bound{(Rank)0, (Raw)0};
   uint32_t step = 0;  // edges and chunks offered so far (selects the append counter)
   const bool pl = p.prefer_larger != 0;
 
-  auto set_bound = [&](Rank tau) {
+  auto set_bound = [&](Rank tau, uint32_t kept) {
     bound.tau = tau;
     bound.raw = TR::unrank(tau, dirmask);
     open = false;
-    count = k;
+    count = kept;
   };
-  // Keep the k best of the list and `n_ext` keys at `ext` (indices idx0..)
-  // in the spare buffer, which becomes the list.
-  auto select_union = [&](const Raw* ext, uint32_t idx0, uint32_t n_ext) {
-    const Rank tau = trim_into<TR, NT>(ctl, Src<Raw>{list_raw, list_idx, count, ext, idx0, n_ext}, spare_raw,
-                                       spare_idx, k, dirmask, pl, cbuf);
+  auto swap_lists = [&]() {
     Raw* tr = list_raw;
     list_raw = spare_raw;
     spare_raw = tr;
     uint32_t* ti = list_idx;
     list_idx = spare_idx;
     spare_idx = ti;
-    set_bound(tau);
   };
-  auto trim_list = [&]() { select_union(nullptr, 0u, 0u); };
+  // Keep the k best of the list and `n_ext` keys at `ext` (indices idx0..)
+  // -- with slack, up to k + slack entries that include them -- in the spare
+  // buffer, which becomes the list.
+  auto select_union = [&](const Raw* ext, uint32_t idx0, uint32_t n_ext, uint32_t slack) {
+    const Kept<Rank> kp = trim_into<TR, NT>(ctl, Src<Raw>{list_raw, list_idx, count, ext, idx0, n_ext}, spare_raw,
+                                            spare_idx, k, slack, dirmask, pl, cbuf);
+    swap_lists();
+    set_bound(kp.max_rank, kp.n);
+  };
+  auto trim_list = [&](uint32_t slack) { select_union(nullptr, 0u, 0u, slack); };
 
   // Offer this thread's U vectors (vector j: vc[j] keys from slot 0, source
   // indices i0[j] + slot). Keys that may beat the bound are tested exactly;
@@ -332,6 +326,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   // of the list and all of those keys.
   auto process_vectors = [&](const uint4* stage, uint32_t v0, uint32_t v1, uint32_t idx0) {
     const Raw* stage_keys = reinterpret_cast<const Raw*>(stage);
+    bool trimmed = false;
     for (;;) {
       const bool overflow = offer_chunk(stage, v0, v1, idx0);
       if (!__syncthreads_or(overflow)) {
@@ -339,10 +334,11 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
         return;
       }
       finish_step(false); // drop this attempt's appends
-      if (count > k) {
-        trim_list();
+      if (!trimmed && count > k) {
+        trim_list(trim_slack);
+        trimmed = true;
       } else {
-        select_union(stage_keys + (size_t)v0 * VK, idx0 + v0 * VK, (v1 - v0) * VK);
+        select_union(stage_keys + (size_t)v0 * VK, idx0 + v0 * VK, (v1 - v0) * VK, trim_slack);
         return;
       }
     }
@@ -350,8 +346,8 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
 
   // Unaligned head / tail keys: plain loads, one per thread.
   auto offer_edge = [&](uint32_t e_begin, uint32_t e_cnt) {
-    if (count + e_cnt > L) // keep room for the edge (never happens with a list of k + 512)
-      trim_list();
+    if (count + e_cnt > L) // keep room for the edge (e_cnt < 8)
+      trim_list(trim_slack);
     uint4 vec[U];
     uint32_t vc[U], i0[U];
 #pragma unroll
@@ -370,68 +366,124 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
     finish_step(true);
   };
 
-  if (has_head && fwd)
-    offer_edge(0, head);
-  if (has_tail && !fwd)
-    offer_edge(n - tail, tail);
-
+  // One pass over this CTA's slice: edges and chunks in preference order.
+  // With allow_spec, the first bound may come from a sample (spec_into):
+  // the sample's share of the slice's k best plus four standard deviations,
+  // so that the list stays small and trims are rare. Returns whether that
+  // speculative bound was used; the caller then checks that the slice gave
+  // at least min(k, n_slice) entries.
+  uint32_t gstep = 0; // ring steps over all passes (stage and mbarrier phase)
   bool copies_ok = true;
-  for (uint32_t s = 0; s < nchunks; ++s) {
-    const uint32_t st = s % S;
-    if (copies_ok)
-      copies_ok = mbar_wait(&ctl.bars[st], (s / S) & 1u);
-    const uint32_t vb = v_lo + chunk_of_step(s) * kChunkVec;
-    const uint32_t nv = min(kChunkVec, v_hi - vb);
-    const uint4* stage = reinterpret_cast<const uint4*>(ring + (size_t)st * kChunkBytes);
-    const Raw* stage_keys = reinterpret_cast<const Raw*>(stage);
-    const uint32_t nkeys = copies_ok ? nv * VK : 0u;
-    const uint32_t idx0 = head + vb * VK;
-    if (open) {
-      if (count + nkeys <= k) {
-        // still fewer than k keys in all: every one of them is selected so far
-        for (uint32_t e = threadIdx.x; e < nkeys; e += NT) {
-          list_raw[count + e] = stage_keys[e];
-          list_idx[count + e] = idx0 + e;
-        }
-        __syncthreads();
-        count += nkeys;
-      } else {
-        // the first bound: the k best of the list and the most preferred keys
-        // of this chunk (enough to pass k, at least kBootKeys); the rest of the
-        // chunk comes later in preference order and is offered against it
-        const uint32_t want = max(k + 1 - count, (uint32_t)kBootKeys);
-        const uint32_t nb = min(nv, (want + VK - 1) / VK);
-        const uint32_t b0 = fwd ? 0u : nv - nb; // first vector of the bootstrap part
-        select_union(stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nb * VK);
-        if (nb < nv)
-          process_vectors(stage, fwd ? nb : 0u, fwd ? nv : nv - nb, idx0);
-      }
-    } else if (copies_ok) {
-      process_vectors(stage, 0u, nv, idx0);
-    }
-    // every read of this stage is over: refill it
-    if (threadIdx.x == 0 && copies_ok && issued < nchunks) {
-      issue(issued);
+  auto stream_pass = [&](bool allow_spec) {
+    bool spec_used = false;
+    const uint32_t gbase = gstep;
+    uint32_t issued = 0;
+    auto issue_next = [&]() {
+      const uint32_t g = gbase + issued;
+      const uint32_t v0 = v_lo + chunk_of_step(issued) * kChunkVec;
+      const uint32_t nv = min(kChunkVec, v_hi - v0);
+      const uint32_t st = g % S;
+      mbar_arrive_expect_tx(&ctl.bars[st], nv * 16u);
+      bulk_load(ring + (size_t)st * kChunkBytes, seg_keys + head + (size_t)v0 * VK, nv * 16u, &ctl.bars[st]);
       ++issued;
+    };
+    if (threadIdx.x == 0 && copies_ok) {
+      while (issued < S && issued < nchunks)
+        issue_next();
     }
-  }
-  if (!copies_ok && threadIdx.x == 0) {
-    // let every copy still in flight land before this CTA's shared memory is released
-    for (uint32_t s = 0; s < issued; ++s)
-      mbar_wait(&ctl.bars[s % S], (s / S) & 1u);
-  }
 
-  if (has_tail && fwd)
-    offer_edge(n - tail, tail);
-  if (has_head && !fwd)
-    offer_edge(0, head);
+    if (has_head && fwd)
+      offer_edge(0, head);
+    if (has_tail && !fwd)
+      offer_edge(n - tail, tail);
+
+    for (uint32_t s = 0; s < nchunks; ++s) {
+      const uint32_t g = gbase + s;
+      const uint32_t st = g % S;
+      if (copies_ok)
+        copies_ok = mbar_wait(&ctl.bars[st], (g / S) & 1u);
+      const uint32_t vb = v_lo + chunk_of_step(s) * kChunkVec;
+      const uint32_t nv = min(kChunkVec, v_hi - vb);
+      const uint4* stage = reinterpret_cast<const uint4*>(ring + (size_t)st * kChunkBytes);
+      const Raw* stage_keys = reinterpret_cast<const Raw*>(stage);
+      const uint32_t nkeys = copies_ok ? nv * VK : 0u;
+      const uint32_t idx0 = head + vb * VK;
+      if (open) {
+        if (count + nkeys <= k) {
+          // still fewer than k keys in all: every one of them is selected so far
+          for (uint32_t e = threadIdx.x; e < nkeys; e += NT) {
+            list_raw[count + e] = stage_keys[e];
+            list_idx[count + e] = idx0 + e;
+          }
+          __syncthreads();
+          count += nkeys;
+        } else {
+          // the first bound, from the list and the most preferred keys of this
+          // chunk (enough to pass k, at least kBootKeys); the rest of the chunk
+          // comes later in preference order and is offered against it
+          const uint32_t want = max(k + 1 - count, (uint32_t)kBootKeys);
+          const uint32_t nb = min(nv, (want + VK - 1) / VK);
+          const uint32_t b0 = fwd ? 0u : nv - nb; // first vector of the sample
+          const uint32_t ns = count + nb * VK;
+          bool done = false;
+          if (allow_spec) {
+            const float mu = (float)k * (float)ns / (float)n_slice;
+            const uint32_t mm = (uint32_t)ceilf(mu + 4.0f * sqrtf(mu) + 3.0f);
+            if (mm < k && mm < ns) {
+              const Spec<Rank> sp =
+                spec_into<TR, NT>(ctl, Src<Raw>{list_raw, list_idx, count, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK,
+                                                nb * VK},
+                                  spare_raw, spare_idx, mm, L, dirmask, cbuf);
+              if (sp.ok) {
+                swap_lists();
+                set_bound(sp.edge + 1, sp.n); // accept rank <= edge
+                spec_used = true;
+                done = true;
+              }
+            }
+          }
+          if (!done)
+            select_union(stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nb * VK, trim_slack);
+          if (nb < nv)
+            process_vectors(stage, fwd ? nb : 0u, fwd ? nv : nv - nb, idx0);
+        }
+      } else if (copies_ok) {
+        process_vectors(stage, 0u, nv, idx0);
+      }
+      // every read of this stage is over: refill it
+      if (threadIdx.x == 0 && copies_ok && issued < nchunks)
+        issue_next();
+    }
+    if (!copies_ok && threadIdx.x == 0) {
+      // let every copy still in flight land before this CTA's shared memory is released
+      for (uint32_t s = 0; s < issued; ++s)
+        mbar_wait(&ctl.bars[(gbase + s) % S], ((gbase + s) / S) & 1u);
+    }
+    gstep = gbase + nchunks;
+
+    if (has_tail && fwd)
+      offer_edge(n - tail, tail);
+    if (has_head && !fwd)
+      offer_edge(0, head);
+    return spec_used;
+  };
+
+  if (stream_pass(true) && count < min(k, n_slice) && copies_ok) {
+    // the sample misled the bound (an ordered slice): read the slice again
+    // with bounds from exact selections only
+    count = 0;
+    open = true;
+    bound = Bound<Raw, Rank>{(Rank)0, (Raw)0};
+    __syncthreads();
+    stream_pass(false);
+  }
 
   // local top-k of this CTA's slice, for clusters that gather top-k lists
   // or merge histograms (a lone CTA, or a cluster that gathers whole lists,
   // selects once when writing the output)
   __syncthreads();
   if (count > k && C > 1 && p.merge_gather != 2)
-    trim_list();
+    trim_list(0u);
 
   Raw* out_keys = reinterpret_cast<Raw*>(p.out_keys) + seg * (int64_t)k;
   int32_t* out_values = p.out_values ? p.out_values + seg * (int64_t)k : nullptr;
@@ -447,7 +499,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
     }
     uint32_t mm = nn; // every entry is selected when nn <= k
     if (nn > k) {
-      trim_into<TR, NT>(ctl, list_src(raw, idx, nn), sp_raw, sp_idx, k, dirmask, pl, cbuf);
+      trim_into<TR, NT>(ctl, list_src(raw, idx, nn), sp_raw, sp_idx, k, 0u, dirmask, pl, cbuf);
       raw = sp_raw;
       idx = sp_idx;
       mm = k;
