@@ -70,7 +70,7 @@ cudaError_t device_info(DeviceInfo* out)
 
 constexpr uint32_t kStages = 2;
 constexpr int64_t kMinSliceKeys = 16384; // a CTA of a multi-CTA cluster reads at least this many keys
-constexpr int kThreads = 256;
+constexpr int kThreads = kCtaThreads;
 
 struct Plan {
   LaunchShape shape;

@@ -10,6 +10,8 @@
 // segment-local source index of every entry, in no particular order.
 #pragma once
 
+#include <cstddef>
+
 #include "common.cuh"
 
 namespace segtopk {
@@ -17,24 +19,46 @@ namespace segtopk {
 constexpr int kDigitBits = 8;
 constexpr int kBuckets = 1 << kDigitBits;
 
+// Per-pass scratch of the digit selection. Passes are counted over every
+// selection a block makes: pass j uses slot j % 3 and clears slot (j+1) % 3,
+// whose last readers finished before the barrier of pass j-1. So a pass
+// needs one barrier, and consecutive selections need none between them. The
+// compaction after a selection uses the slot of its last pass (kept, kmax),
+// which the second pass of the next selection clears.
+struct __align__(16) PassSlot {
+  uint32_t hist[kBuckets]; // digit histogram (read with 16-byte loads)
+  uint32_t and_w[2];       // AND / OR of the keys seen (one or two words)
+  uint32_t or_w[2];
+  uint32_t ncand;          // candidates stored in the position buffer
+  uint32_t kept;           // compaction: entries written so far
+  uint32_t nfin;           // counting finish: keys staged
+  unsigned long long kmax; // compaction: largest rank written
+};
+
+// Keys a warp gathers for the counting finish of a selection.
+constexpr uint32_t kFinishMax = 64;
+
 // Control block at the start of dynamic shared memory. Every CTA of a cluster
 // has the same layout, so a field can be addressed in a peer through DSMEM.
 struct Ctrl {
-  uint64_t bars[8];               // one mbarrier per ring stage
-  uint64_t scan_tot[2][32];       // per-warp packed totals of the block scans (double buffered)
-  uint64_t red[32];               // block reductions
-  uint32_t hist[2][kBuckets];     // digit histograms (double buffered; zero outside a selection)
-  uint32_t hist_merged[kBuckets]; // cluster leader: histogram pushed by the other CTAs
-  uint32_t res[4];                // selection result of a pass: bucket, count before, bucket count
-  uint32_t sel_and[2][2];         // selection: AND of keys seen in passes 0 / 1 (one or two words)
-  uint32_t sel_or[2][2];          // selection: OR of keys seen in passes 0 / 1
-  uint32_t sel_ncand;             // selection: candidates stored in the position buffer
-  uint32_t kept;                  // compaction: entries written so far
-  uint32_t chunk_count[3];        // entries appended during a chunk (three in rotation)
-  uint32_t gather_count;          // cluster leader: entries gathered from the cluster
-  uint32_t front_base;            // cross-CTA scan: selected entries of preceding CTAs
-  uint32_t tie_base;              // cross-CTA scan: boundary ties of preceding CTAs
+  uint64_t bars[8];                  // one mbarrier per ring stage
+  uint64_t scan_tot[2][32];          // per-warp packed totals of the block scans (double buffered)
+  uint64_t red[32];                  // block reductions
+  PassSlot slot[3];                  // digit selection passes (see PassSlot)
+  uint64_t fin[kFinishMax];          // staging of the counting finish
+  uint32_t hist_m0[kBuckets];        // cluster histogram merge: this CTA's histogram
+  uint32_t hist_merged[kBuckets];    // cluster leader: histogram pushed by the other CTAs
+  uint32_t res[4];                   // cluster leader: result of a merged pass
+  uint32_t chunk_count[3];           // entries appended during a chunk (three in rotation)
+  uint32_t gather_count;             // cluster leader: entries gathered from the cluster
+  uint32_t front_base;               // cross-CTA scan: selected entries of preceding CTAs
+  uint32_t tie_base;                 // cross-CTA scan: boundary ties of preceding CTAs
+  uint64_t xb[16][2];                // cluster leader: every CTA's local k-th (rank, preference index)
+  uint64_t xb_min[2];                // the cluster-wide minimum of xb
 };
+static_assert(sizeof(PassSlot) % 16 == 0, "every slot's histogram is 16-byte aligned");
+static_assert(offsetof(Ctrl, slot) % 16 == 0, "the slots are 16-byte aligned");
+static_assert(offsetof(PassSlot, kmax) % 8 == 0, "64-bit shared atomics need 8-byte alignment");
 constexpr uint32_t kCtrlBytes = (sizeof(Ctrl) + 127u) & ~127u;
 
 // Entries a selection reads: `count` list entries, then `ext_count` keys of
@@ -61,16 +85,6 @@ __device__ __forceinline__ Src<Raw> list_src(const Raw* raw, const uint32_t* idx
 // Warp 0 of the block: find the bucket holding the krem-th best candidate.
 // `h` holds the 8 bucket counts this lane owns (buckets 8*lane .. 8*lane+7).
 // Writes bucket, count before it and its count to res[].
-__device__ __forceinline__ void find_bucket(const uint32_t (&h)[8], uint32_t krem, uint32_t* res);
-// The same, reading the lane's 8 counts from a 16-byte aligned histogram with
-// two conflict-free 16-byte loads.
-__device__ __forceinline__ void find_bucket_in(const uint32_t* hist, uint32_t krem, uint32_t* res)
-{
-  const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 2 * lane_id();
-  const uint4 a = h4[0], b = h4[1];
-  const uint32_t h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-  find_bucket(h, krem, res);
-}
 __device__ __forceinline__ void find_bucket(const uint32_t (&h)[8], uint32_t krem, uint32_t* res)
 {
   const uint32_t lane = lane_id();
@@ -97,6 +111,35 @@ __device__ __forceinline__ void find_bucket(const uint32_t (&h)[8], uint32_t kre
     res[1] = before;
     res[2] = cnt;
   }
+}
+
+// Every lane of the calling warp: the bucket of `hist` (16-byte aligned)
+// holding the krem-th best candidate, the count before it and its count.
+__device__ __forceinline__ void find_bucket_warp(const uint32_t* hist, uint32_t krem, uint32_t& b, uint32_t& before,
+                                                 uint32_t& cnt)
+{
+  const uint32_t lane = lane_id();
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist) + 2 * lane;
+  const uint4 x = h4[0], y = h4[1];
+  const uint32_t h[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+  const uint32_t sum = (h[0] + h[1]) + (h[2] + h[3]) + (h[4] + h[5]) + (h[6] + h[7]);
+  const uint32_t incl = warp_inclusive_sum(sum);
+  const uint32_t src = __ffs(__ballot_sync(kFull, incl >= krem)) - 1; // the candidate total is always >= krem
+  // within the source lane: the first of its buckets that reaches krem
+  uint32_t cum = incl - sum, bb = 7, bf = 0, bc = 0;
+  bool got = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool hit = !got && cum + h[i] >= krem;
+    bb = hit ? (uint32_t)i : bb;
+    bf = hit ? cum : bf;
+    bc = hit ? h[i] : bc;
+    got |= hit;
+    cum += h[i];
+  }
+  b = 8 * src + __shfl_sync(kFull, bb, src);
+  before = __shfl_sync(kFull, bf, src);
+  cnt = __shfl_sync(kFull, bc, src);
 }
 
 template <class Key>
@@ -141,66 +184,68 @@ __device__ __forceinline__ Key read_word(const uint32_t* w)
     return (Key)w[0];
 }
 
-// Boundary candidates left at which a selection switches to counting.
-constexpr uint32_t kFinishMax = 64;
-
-// Warp 0: the candidates (positions pos[0..npos)) whose key matches r's
-// prefix -- at most kFinishMax of them -- are gathered, and the krem-th
-// best key value v among them is found by counting. Writes v (one or two
-// words) to res[0..1], the number of candidates better than v to res[2] and
-// the number equal to v to res[3]. Uses ctl.scan_tot as staging.
-template <class Key, class Get>
-__device__ void finish_by_count(Ctrl& ctl, const uint16_t* pos, uint32_t npos, const Radix<Key>& r, Get&& get)
+// Clears a pass slot (block-wide part: histogram words by thread index).
+template <int NT>
+__device__ __forceinline__ void clear_slot(PassSlot& sl)
 {
-  Key* small = reinterpret_cast<Key*>(&ctl.scan_tot[0][0]); // 64 keys
-  const uint32_t lane = lane_id();
-  uint32_t n = 0;
-  for (uint32_t base = 0; base < npos; base += 32) {
-    const uint32_t i = base + lane;
-    Key key = 0;
-    bool on = false;
-    if (i < npos)
-      on = get((uint32_t)pos[i], key) && (key & r.mask) == r.prefix;
-    const uint32_t bal = __ballot_sync(kFull, on);
-    const uint32_t slot = n + __popc(bal & lanemask_lt());
-    if (on && slot < kFinishMax)
-      small[slot] = key;
-    n += __popc(bal);
-  }
-  __syncwarp();
-  if (n > kFinishMax)
-    n = kFinishMax; // cannot happen: the caller checked the bucket count
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint32_t i = lane + 32u * (uint32_t)q;
-    const Key v = i < n ? small[i] : (Key)0;
-    uint32_t less = 0, eq = 0;
-    for (uint32_t j = 0; j < n; ++j) {
-      const Key w = small[j];
-      less += w < v ? 1u : 0u;
-      eq += w == v ? 1u : 0u;
-    }
-    if (i < n && less < r.krem && r.krem <= less + eq) {
-      // every lane holding this value writes the same result
-      if constexpr (sizeof(Key) == 8) {
-        ctl.res[0] = (uint32_t)v;
-        ctl.res[1] = (uint32_t)(v >> 32);
-      } else {
-        ctl.res[0] = (uint32_t)v;
-      }
-      ctl.res[2] = less;
-      ctl.res[3] = eq;
-    }
+  for (uint32_t i = threadIdx.x; i < (uint32_t)kBuckets; i += NT)
+    sl.hist[i] = 0;
+  if (threadIdx.x == 0) {
+    sl.and_w[0] = sl.and_w[1] = ~0u;
+    sl.or_w[0] = sl.or_w[1] = 0u;
+    sl.ncand = 0;
+    sl.kept = 0;
+    sl.nfin = 0;
+    sl.kmax = 0;
   }
 }
 
-// Resets the selection scratch (called before a selection's first barrier by
-// thread 0 of a block that has passed a barrier since the last selection).
-__device__ __forceinline__ void reset_select_scratch(Ctrl& ctl)
+// Counting finish of a selection, block-wide: the candidates (positions
+// pos[0..npos)) whose key matches prefix under mask -- at most kFinishMax of
+// them -- are staged in shared memory (counter *nfin, zero on entry); after
+// one barrier every warp finds, by counting over registers and shuffles, the
+// krem-th best key value v among them, the number of staged keys better
+// than v and the number equal to it.
+template <class Key, int NT, class Get>
+__device__ __forceinline__ void finish_by_count(Key* stage, uint32_t* nfin, const uint16_t* pos, uint32_t npos,
+                                                Key prefix, Key mask, uint32_t krem, Get&& get, Key& v, uint32_t& less,
+                                                uint32_t& eq)
 {
-  ctl.sel_ncand = 0;
-  ctl.sel_and[0][0] = ctl.sel_and[0][1] = ctl.sel_and[1][0] = ctl.sel_and[1][1] = ~0u;
-  ctl.sel_or[0][0] = ctl.sel_or[0][1] = ctl.sel_or[1][0] = ctl.sel_or[1][1] = 0u;
+  for (uint32_t i = threadIdx.x; i < npos; i += NT) {
+    Key key = 0;
+    if (get((uint32_t)pos[i], key) && (key & mask) == prefix) {
+      const uint32_t slot = atomicAdd(nfin, 1u);
+      if (slot < kFinishMax)
+        stage[slot] = key;
+    }
+  }
+  __syncthreads();
+  uint32_t n = *nfin;
+  if (n > kFinishMax)
+    n = kFinishMax; // cannot happen: the caller checked the bucket count
+  const uint32_t lane = lane_id();
+  const Key a = lane < n ? stage[lane] : (Key)0;
+  const Key c = lane + 32 < n ? stage[lane + 32] : (Key)0;
+  uint32_t la = 0, ea = 0, lc = 0, ec = 0;
+#pragma unroll 8
+  for (uint32_t j = 0; j < 32; ++j) {
+    const Key w0 = __shfl_sync(kFull, a, j);
+    const Key w1 = __shfl_sync(kFull, c, j);
+    const bool in0 = j < n, in1 = j + 32 < n;
+    la += (in0 & (w0 < a)) + (in1 & (w1 < a));
+    ea += (in0 & (w0 == a)) + (in1 & (w1 == a));
+    lc += (in0 & (w0 < c)) + (in1 & (w1 < c));
+    ec += (in0 & (w0 == c)) + (in1 & (w1 == c));
+  }
+  const bool fa = lane < n && la < krem && krem <= la + ea;
+  const bool fc = lane + 32 < n && lc < krem && krem <= lc + ec;
+  const uint32_t bal = __ballot_sync(kFull, fa || fc);
+  const uint32_t src = bal ? __ffs(bal) - 1 : 0u;
+  const Key mine = fa ? a : c;
+  const uint32_t ml = fa ? la : lc, me = fa ? ea : ec;
+  v = __shfl_sync(kFull, mine, src);
+  less = __shfl_sync(kFull, ml, src);
+  eq = __shfl_sync(kFull, me, src);
 }
 
 // One radix selection: among the candidates (get(e, key) returns true) of
@@ -210,7 +255,8 @@ __device__ __forceinline__ void reset_select_scratch(Ctrl& ctl)
 // finds the bucket holding the krem-th best, narrows krem and folds the digit
 // into the prefix; it stops when that bucket holds exactly krem candidates
 // ("Implement Segmented TopK using Thread-Block-Clusters", sections 1.2
-// "Radix (digit) top-k" and 1.4 "Early stop"). With slack > 0 it also stops
+// "Radix (digit) top-k" and 1.4 "Early stop"). With slack > 0 it also stops,
+// from the second digit on (a first-digit bucket is too coarse a bound),
 // once the bucket holds at most krem + slack candidates: taking the whole
 // bucket then keeps between kk and kk + slack candidates, all of them at
 // least as good as every candidate left out. A pass after the first that
@@ -220,14 +266,14 @@ __device__ __forceinline__ void reset_select_scratch(Ctrl& ctl)
 //
 // Work saving: pass 0 also records the AND / OR of every candidate key and
 // pass 1 those of the remaining candidates, together with their positions
-// in `cb` when they fit; later passes then visit only those positions, and a
-// digit on which all remaining candidates agree is folded without a pass.
-// Each thread takes 4 entries per loop trip, loads first.
-// Requires at least kk candidates. Block-wide; the selection scratch must be
-// reset (reset_select_scratch) and is reset again on return; both
-// histograms are zero before and after.
+// in `cb` when they fit; later passes then visit only those positions, a
+// digit on which all remaining candidates agree is folded without a pass,
+// and at most kFinishMax boundary candidates are resolved by counting.
+// Each pass takes one barrier: every warp finds the bucket itself. `pass`
+// is the block's pass counter (see PassSlot). Requires at least kk
+// candidates. Block-wide.
 template <class Key, int KEY_BITS, int NT, class Get>
-__device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* dom, uint32_t dom_n,
+__device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t& pass, uint32_t count, const uint16_t* dom, uint32_t dom_n,
                                    uint32_t kk, uint32_t slack, uint32_t abort_cnt, CandBuf& cb, Get&& get)
 {
   constexpr int P = KEY_BITS / kDigitBits;
@@ -236,9 +282,9 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* do
   const uint32_t span = dom ? dom_n : count;
   const bool can_compact = cb.pos != nullptr;
   bool compacted = false;
+  uint32_t ncand = 0;
   Key diff = ~(Key)0; // digits that may differ among the remaining candidates
   Key kand_v = 0;
-  int hb = 0;         // histogram buffer of the current pass
   for (int p = 0; p < P; ++p) {
     const int shift = KEY_BITS - kDigitBits * (p + 1);
     const Key dmask = (Key)(kBuckets - 1) << shift;
@@ -248,10 +294,11 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* do
       r.mask |= dmask;
       continue;
     }
-    uint32_t* h = ctl.hist[hb];
+    PassSlot& sl = ctl.slot[pass % 3];
+    uint32_t* h = sl.hist;
     const bool rec = p <= 1; // record AND / OR
     const bool collect = p == 1 && can_compact;
-    const uint32_t n_visit = compacted ? ctl.sel_ncand : span;
+    const uint32_t n_visit = compacted ? ncand : span;
     Key ta = ~(Key)0, to = (Key)0;
     for (uint32_t base = 0; base < n_visit; base += NT * UNR) {
       Key key[UNR];
@@ -279,7 +326,7 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* do
         }
       }
       if (collect && nc) {
-        uint32_t slot = atomicAdd(&ctl.sel_ncand, nc);
+        uint32_t slot = atomicAdd(&sl.ncand, nc);
 #pragma unroll
         for (int u = 0; u < UNR; ++u) {
           if (on[u]) {
@@ -291,53 +338,46 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t count, const uint16_t* do
       }
     }
     if (rec)
-      fold_and_or(ctl.sel_and[p], ctl.sel_or[p], ta, to);
-    if (threadIdx.x < kBuckets)
-      ctl.hist[hb ^ 1][threadIdx.x] = 0;
+      fold_and_or(sl.and_w, sl.or_w, ta, to);
+    clear_slot<NT>(ctl.slot[(pass + 1) % 3]);
     __syncthreads();
-    if (threadIdx.x < 32)
-      find_bucket_in(h, r.krem, ctl.res);
-    __syncthreads();
-    const uint32_t b = ctl.res[0], before = ctl.res[1], cnt = ctl.res[2];
+    uint32_t b, before, cnt;
+    find_bucket_warp(h, r.krem, b, before, cnt);
     if (rec) {
-      kand_v = read_word<Key>(ctl.sel_and[p]);
-      diff = kand_v ^ read_word<Key>(ctl.sel_or[p]);
+      kand_v = read_word<Key>(sl.and_w);
+      diff = kand_v ^ read_word<Key>(sl.or_w);
     }
-    if (collect)
-      compacted = ctl.sel_ncand <= cb.cap;
+    if (collect) {
+      ncand = sl.ncand;
+      compacted = ncand <= cb.cap;
+    }
+    ++pass;
     r.krem -= before;
     r.cnt = cnt;
     r.prefix |= (Key)b << shift;
     r.mask |= dmask;
-    if (threadIdx.x < kBuckets)
-      h[threadIdx.x] = 0; // warp 0 read it before the barrier above
-    hb ^= 1;
-    if (cnt - r.krem <= slack) {
+    if (cnt == r.krem || (p >= 1 && cnt - r.krem <= slack)) {
       r.stopped = true;
       break;
     }
     if (p >= 1 && cnt > abort_cnt)
       break;
     if (compacted && cnt <= kFinishMax && p + 1 < P) {
-      // few candidates left: resolve the boundary key by counting (warp 0)
-      __syncthreads(); // everyone has read ctl.res
-      if (threadIdx.x < 32)
-        finish_by_count<Key>(ctl, cb.pos, ctl.sel_ncand, r, get);
-      __syncthreads();
-      r.prefix = read_word<Key>(ctl.res);
+      // few candidates left: resolve the boundary key by counting (the slot
+      // of the pass just done holds the staging counter)
+      Key v;
+      uint32_t less, eq;
+      finish_by_count<Key, NT>(reinterpret_cast<Key*>(ctl.fin), &ctl.slot[(pass + 2) % 3].nfin, cb.pos, ncand,
+                               r.prefix, r.mask, r.krem, get, v, less, eq);
+      r.prefix = v;
       r.mask = ~(Key)0;
-      r.krem -= ctl.res[2];
-      r.cnt = ctl.res[3];
-      r.stopped = r.cnt - r.krem <= slack;
+      r.krem -= less;
+      r.cnt = eq;
+      r.stopped = eq - r.krem <= slack;
       break;
     }
-    // ctl.res and h are rewritten only after the next barrier
   }
-  cb.n = compacted ? ctl.sel_ncand : ~0u;
-  __syncthreads(); // everyone has read the scratch
-  if (threadIdx.x == 0)
-    reset_select_scratch(ctl);
-  __syncthreads(); // histograms zero and scratch reset for the next selection
+  cb.n = compacted ? ncand : ~0u;
   return r;
 }
 
@@ -355,6 +395,7 @@ template <class Rank>
 struct Selection {
   Rank prefix, mask;
   uint32_t iprefix, imask;
+  uint32_t n; // entries selected
   // 0: not selected, 1: front, 2: selected boundary entry
   __device__ __forceinline__ int classify(Rank r, uint32_t pidx) const
   {
@@ -371,7 +412,7 @@ struct Selection {
 // the rank selection left the boundary candidates in `cb`, only those are
 // visited.
 template <class TR, int NT>
-__device__ void select_ties(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_t q,
+__device__ void select_ties(Ctrl& ctl, uint32_t& pass, const Src<typename TR::Raw>& src, uint32_t q,
                             typename TR::Rank dirmask, bool prefer_larger, Selection<typename TR::Rank>& s,
                             CandBuf& cb)
 {
@@ -380,7 +421,7 @@ __device__ void select_ties(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_
   const bool use = cb.pos != nullptr && cb.n != ~0u;
   CandBuf none{nullptr, 0u, ~0u};
   const Radix<uint32_t> ri = radix_select<uint32_t, 32, NT>(
-    ctl, src.size(), use ? cb.pos : nullptr, use ? cb.n : 0u, q, 0u, ~0u, use ? none : cb, [&](uint32_t e, uint32_t& key) {
+    ctl, pass, src.size(), use ? cb.pos : nullptr, use ? cb.n : 0u, q, 0u, ~0u, use ? none : cb, [&](uint32_t e, uint32_t& key) {
       key = pref_index(src.index(e), prefer_larger);
       return (TR::rank(src.key(e), dirmask) & mask) == prefix;
     });
@@ -393,19 +434,21 @@ __device__ void select_ties(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_
 // radix selection on the rank code, then, if more boundary entries tie than
 // are needed, one on the preference index.
 template <class TR, int NT>
-__device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_t kk,
-                                                     uint32_t slack, typename TR::Rank dirmask, bool prefer_larger,
-                                                     CandBuf cb)
+__device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, uint32_t& pass, const Src<typename TR::Raw>& src,
+                                                     uint32_t kk, uint32_t slack, typename TR::Rank dirmask,
+                                                     bool prefer_larger, CandBuf cb)
 {
   using Rank = typename TR::Rank;
-  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, src.size(), nullptr, 0u, kk, slack, ~0u, cb,
+  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, pass, src.size(), nullptr, 0u, kk, slack, ~0u, cb,
                                                                [&](uint32_t e, Rank& key) {
                                                                  key = TR::rank(src.key(e), dirmask);
                                                                  return true;
                                                                });
-  Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u};
-  if (!rr.stopped) // every rank digit resolved and more than krem entries share the boundary rank
-    select_ties<TR, NT>(ctl, src, rr.krem, dirmask, prefer_larger, s, cb);
+  Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u, kk};
+  if (rr.stopped) // the whole boundary bucket is taken
+    s.n = kk - rr.krem + rr.cnt;
+  else // every rank digit resolved and more than krem entries share the boundary rank
+    select_ties<TR, NT>(ctl, pass, src, rr.krem, dirmask, prefer_larger, s, cb);
   return s;
 }
 
@@ -499,18 +542,59 @@ __device__ __forceinline__ Rank block_max(Ctrl& ctl, Rank v)
   return m;
 }
 
-// Entries kept by a compaction: their number and their largest rank.
+// The worst (largest (rank, preference index)) of `count` list entries.
+// Block-wide; every thread gets the result.
+template <class TR, int NT>
+__device__ __forceinline__ void list_worst(Ctrl& ctl, const typename TR::Raw* raw, const uint32_t* idx,
+                                           uint32_t count, typename TR::Rank dirmask, bool prefer_larger,
+                                           uint64_t& w_rank, uint64_t& w_pidx)
+{
+  using Rank = typename TR::Rank;
+  if constexpr (TR::kRankBits <= 32) {
+    uint64_t mx = 0;
+    for (uint32_t e = threadIdx.x; e < count; e += NT) {
+      const uint64_t c = ((uint64_t)TR::rank(raw[e], dirmask) << 32) | pref_index(idx[e], prefer_larger);
+      mx = c > mx ? c : mx;
+    }
+    mx = block_max<uint64_t, NT>(ctl, mx);
+    w_rank = mx >> 32;
+    w_pidx = mx & 0xffffffffull;
+  } else {
+    Rank mr = 0;
+    for (uint32_t e = threadIdx.x; e < count; e += NT) {
+      const Rank r = TR::rank(raw[e], dirmask);
+      mr = r > mr ? r : mr;
+    }
+    mr = block_max<Rank, NT>(ctl, mr);
+    uint32_t mp = 0;
+    for (uint32_t e = threadIdx.x; e < count; e += NT) {
+      const uint32_t pi = pref_index(idx[e], prefer_larger);
+      if (TR::rank(raw[e], dirmask) == mr)
+        mp = pi > mp ? pi : mp;
+    }
+    mp = block_max<uint32_t, NT>(ctl, mp);
+    w_rank = (uint64_t)mr;
+    w_pidx = mp;
+  }
+}
+
+// Entries kept by a compaction: their number and their largest rank, and
+// the block's pass counter after the selection.
 template <class Rank>
 struct Kept {
   Rank max_rank;
   uint32_t n;
+  uint32_t pass;
 };
 
 // Writes the entries of `src` that `s` selects to dst[0, cap) in no
-// particular order (warp-aggregated atomic positions, one pass, no scan).
-// dst must not overlap src's arrays. Block-wide.
+// particular order (warp-aggregated atomic positions, one pass, no scan),
+// and returns their number and largest rank. `pass` is the pass counter
+// after the selection: the slot of its last pass holds the counters. dst
+// must not overlap src's arrays. Block-wide; ends with a barrier.
 template <class TR, int NT>
-__device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, const Src<typename TR::Raw>& src,
+__device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, uint32_t pass,
+                                                               const Src<typename TR::Raw>& src,
                                                                const Selection<typename TR::Rank>& s,
                                                                typename TR::Raw* dst_raw, uint32_t* dst_idx,
                                                                uint32_t cap, typename TR::Rank dirmask,
@@ -518,9 +602,7 @@ __device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, const 
 {
   using Raw = typename TR::Raw;
   using Rank = typename TR::Rank;
-  if (threadIdx.x == 0)
-    ctl.kept = 0;
-  __syncthreads();
+  PassSlot& sl = ctl.slot[(pass + 2) % 3];
   Rank mx = 0;
   const uint32_t n = src.size();
   for (uint32_t base = 0; base < n; base += NT) {
@@ -539,7 +621,7 @@ __device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, const 
     if (bal) {
       uint32_t wb = 0;
       if (lane_id() == 0)
-        wb = atomicAdd(&ctl.kept, __popc(bal));
+        wb = atomicAdd(&sl.kept, __popc(bal));
       const uint32_t pos = __shfl_sync(kFull, wb, 0) + __popc(bal & lanemask_lt());
       if (keep && pos < cap) { // pos < cap always holds for a valid selection; guards dst
         dst_raw[pos] = kr;
@@ -548,9 +630,11 @@ __device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, const 
       }
     }
   }
-  const Rank bm = block_max<Rank, NT>(ctl, mx); // its barriers also publish dst and ctl.kept
-  const uint32_t kept = ctl.kept;
-  return Kept<Rank>{bm, kept < cap ? kept : cap};
+  mx = warp_max(mx);
+  if (lane_id() == 0 && mx != 0)
+    atomicMax(&sl.kmax, (unsigned long long)mx);
+  __syncthreads(); // publishes dst and the counters
+  return Kept<Rank>{(Rank)sl.kmax, s.n < cap ? s.n : cap, pass};
 }
 
 // Keep the kk best entries of `src` (size > kk > 0) -- with slack > 0,
@@ -559,13 +643,14 @@ __device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, const 
 // keys (which come after every kept one in preference order) are accepted
 // only below it.
 template <class TR, int NT>
-__device__ __noinline__ Kept<typename TR::Rank> trim_into(Ctrl& ctl, const Src<typename TR::Raw> src,
+__device__ __noinline__ Kept<typename TR::Rank> trim_into(Ctrl& ctl, uint32_t pass, const Src<typename TR::Raw> src,
                                                           typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t kk,
                                                           uint32_t slack, typename TR::Rank dirmask,
                                                           bool prefer_larger, CandBuf cb)
 {
-  const Selection<typename TR::Rank> s = block_select<TR, NT>(ctl, src, kk, slack, dirmask, prefer_larger, cb);
-  return select_into<TR, NT>(ctl, src, s, dst_raw, dst_idx, kk + slack, dirmask, prefer_larger);
+  const Selection<typename TR::Rank> s =
+    block_select<TR, NT>(ctl, pass, src, kk, slack, dirmask, prefer_larger, cb);
+  return select_into<TR, NT>(ctl, pass, src, s, dst_raw, dst_idx, kk + slack, dirmask, prefer_larger);
 }
 
 // A speculative first bound from a sample of a slice: the smallest rank
@@ -583,26 +668,27 @@ struct Spec {
   bool ok;
   Rank edge;
   uint32_t n;
+  uint32_t pass;
 };
 template <class TR, int NT>
-__device__ __noinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, const Src<typename TR::Raw> src,
+__device__ __noinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t pass, const Src<typename TR::Raw> src,
                                                           typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t mm,
                                                           uint32_t cap, typename TR::Rank dirmask, CandBuf cb)
 {
   using Rank = typename TR::Rank;
   constexpr Rank kWorst = (TR::kRankBits == 64) ? ~(Rank)0 : (Rank)(((uint64_t)1 << TR::kRankBits) - 1);
-  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, src.size(), nullptr, 0u, mm, mm, 8u * mm + 64u, cb,
-                                                               [&](uint32_t e, Rank& key) {
+  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, pass, src.size(), nullptr, 0u, mm, mm,
+                                                               8u * mm + 64u, cb, [&](uint32_t e, Rank& key) {
                                                                  key = TR::rank(src.key(e), dirmask);
                                                                  return true;
                                                                });
   const Rank edge = rr.prefix | (~rr.mask & kWorst);
   const uint32_t total = mm - rr.krem + rr.cnt;
   if (!rr.stopped || edge == kWorst || total > cap)
-    return Spec<Rank>{false, (Rank)0, 0u};
-  const Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u}; // the whole boundary bucket
-  const Kept<Rank> kp = select_into<TR, NT>(ctl, src, s, dst_raw, dst_idx, cap, dirmask, false);
-  return Spec<Rank>{true, edge, kp.n};
+    return Spec<Rank>{false, (Rank)0, 0u, pass};
+  const Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u, total}; // the whole boundary bucket
+  const Kept<Rank> kp = select_into<TR, NT>(ctl, pass, src, s, dst_raw, dst_idx, cap, dirmask, false);
+  return Spec<Rank>{true, edge, kp.n, pass};
 }
 
 // ---------------------------------------------------------------------------

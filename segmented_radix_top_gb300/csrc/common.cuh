@@ -145,6 +145,12 @@ __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr)
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ uint64_t dsmem_ld_u64(uint32_t addr)
+{
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void dsmem_st(uint32_t addr, uint16_t v)
 {
   asm volatile("st.shared::cluster.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");

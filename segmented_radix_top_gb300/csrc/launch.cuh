@@ -99,8 +99,8 @@ inline cudaError_t read_and_clear(uint32_t* word)
   const KeyOps& key_ops_##NAME()                                                                   \
   {                                                                                                \
     static const KeyOps ops = {(int)sizeof(KeyTraits<KIND>::Raw), KeyTraits<KIND>::kRankBits,     \
-                               &StreamLauncher<KIND, 256>::launch,                                 \
-                               &StreamLauncher<KIND, 256>::occupancy, &read_and_clear};            \
+                               &StreamLauncher<KIND, kCtaThreads>::launch,                         \
+                               &StreamLauncher<KIND, kCtaThreads>::occupancy, &read_and_clear};    \
     return ops;                                                                                    \
   }                                                                                                \
   }

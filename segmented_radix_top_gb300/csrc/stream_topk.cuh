@@ -33,7 +33,12 @@
 
 namespace segtopk {
 
-constexpr uint32_t kChunkBytes = 32768;
+// Threads per CTA, CTAs an SM is sized for, and 16-byte vectors a thread
+// filters per ring stage (one stage = kCtaThreads * kVecPerThread vectors).
+constexpr int kCtaThreads = 256;
+constexpr int kCtasPerSm = 2;
+constexpr int kVecPerThread = 8;
+constexpr uint32_t kChunkBytes = 16u * (uint32_t)kVecPerThread * (uint32_t)kCtaThreads;
 
 struct KernelParams {
   const void* keys;
@@ -68,7 +73,7 @@ constexpr uint32_t kCandCap = 4096;
 constexpr uint32_t kCandBytes = kCandCap * 2u;
 
 template <KeyKind KK, int NT>
-__global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p)
+__global__ void __launch_bounds__(NT, kCtasPerSm) stream_topk_kernel(const KernelParams p)
 {
   using TR = KeyTraits<KK>;
   using Raw = typename TR::Raw;
@@ -117,13 +122,14 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
 
   // ---- front-loaded shared-memory initialisation ----
   for (uint32_t i = threadIdx.x; i < kBuckets; i += NT) {
-    ctl.hist[0][i] = 0;
-    ctl.hist[1][i] = 0;
+    ctl.hist_m0[i] = 0;
     ctl.hist_merged[i] = 0;
   }
+  clear_slot<NT>(ctl.slot[0]);
+  clear_slot<NT>(ctl.slot[1]);
+  clear_slot<NT>(ctl.slot[2]);
   if (threadIdx.x == 0) {
     ctl.chunk_count[0] = ctl.chunk_count[1] = ctl.chunk_count[2] = 0;
-    reset_select_scratch(ctl);
     ctl.gather_count = 0;
     ctl.front_base = 0;
     ctl.tie_base = 0;
@@ -157,6 +163,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   bool open = true;   // no bound yet: every key is accepted
   Bound<Raw, Rank> bound{(Rank)0, (Raw)0};
   uint32_t step = 0;  // edges and chunks offered so far (selects the append counter)
+  uint32_t sel_pass = 0; // digit-selection passes so far (selects the pass slot)
   const bool pl = p.prefer_larger != 0;
 
   auto set_bound = [&](Rank tau, uint32_t kept) {
@@ -177,8 +184,9 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   // -- with slack, up to k + slack entries that include them -- in the spare
   // buffer, which becomes the list.
   auto select_union = [&](const Raw* ext, uint32_t idx0, uint32_t n_ext, uint32_t slack) {
-    const Kept<Rank> kp = trim_into<TR, NT>(ctl, Src<Raw>{list_raw, list_idx, count, ext, idx0, n_ext}, spare_raw,
-                                            spare_idx, k, slack, dirmask, pl, cbuf);
+    const Kept<Rank> kp = trim_into<TR, NT>(ctl, sel_pass, Src<Raw>{list_raw, list_idx, count, ext, idx0, n_ext},
+                                            spare_raw, spare_idx, k, slack, dirmask, pl, cbuf);
+    sel_pass = kp.pass;
     swap_lists();
     set_bound(kp.max_rank, kp.n);
   };
@@ -431,9 +439,11 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
             const uint32_t mm = (uint32_t)ceilf(mu + 4.0f * sqrtf(mu) + 3.0f);
             if (mm < k && mm < ns) {
               const Spec<Rank> sp =
-                spec_into<TR, NT>(ctl, Src<Raw>{list_raw, list_idx, count, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK,
-                                                nb * VK},
+                spec_into<TR, NT>(ctl, sel_pass,
+                                  Src<Raw>{list_raw, list_idx, count, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK,
+                                           nb * VK},
                                   spare_raw, spare_idx, mm, L, dirmask, cbuf);
+              sel_pass = sp.pass;
               if (sp.ok) {
                 swap_lists();
                 set_bound(sp.edge + 1, sp.n); // accept rank <= edge
@@ -499,7 +509,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
     }
     uint32_t mm = nn; // every entry is selected when nn <= k
     if (nn > k) {
-      trim_into<TR, NT>(ctl, list_src(raw, idx, nn), sp_raw, sp_idx, k, 0u, dirmask, pl, cbuf);
+      sel_pass = trim_into<TR, NT>(ctl, sel_pass, list_src(raw, idx, nn), sp_raw, sp_idx, k, 0u, dirmask, pl, cbuf).pass;
       raw = sp_raw;
       idx = sp_idx;
       mm = k;
@@ -524,10 +534,48 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
 
   // ---------------- cluster merge ----------------
   const uint32_t leader = 0;
-  cluster_sync(); // every CTA has finished streaming; every CTA's initialisation is visible
+  // A CTA holding its slice's exact top-k knows that the segment's k-th best
+  // is no worse than its own k-th best; the best of these bounds over the
+  // cluster limits what every CTA sends to the leader (worth its cost when
+  // the gathered lists would be too long to finish by counting).
+  const bool prune = p.merge_gather == 1 && C * k > kCountMax;
+  if (prune) {
+    uint64_t wr = ~0ull, wp = ~0ull; // no bound
+    if (count >= k)
+      list_worst<TR, NT>(ctl, list_raw, list_idx, count, dirmask, pl, wr, wp);
+    if (threadIdx.x == 0) {
+      const uint32_t xa = dsmem_map(smem_addr(&ctl.xb[rank][0]), leader);
+      dsmem_st(xa, wr);
+      dsmem_st(xa + 8u, wp);
+    }
+  }
+  cluster_sync(); // every CTA has finished streaming and published its bound; every initialisation is visible
 
   if (p.merge_gather) {
-    // every CTA's list (<= k entries) into the leader's ring, one warp-wide atomic per 32 entries
+    if (threadIdx.x < 32) {
+      uint64_t br = ~0ull, bp = ~0ull; // no bound
+      if (prune && threadIdx.x < C) {
+        const uint32_t xa = dsmem_map(smem_addr(&ctl.xb[threadIdx.x][0]), leader);
+        br = dsmem_ld_u64(xa);
+        bp = dsmem_ld_u64(xa + 8u);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t orr = __shfl_xor_sync(kFull, br, o);
+        const uint64_t opp = __shfl_xor_sync(kFull, bp, o);
+        if (orr < br || (orr == br && opp < bp)) {
+          br = orr;
+          bp = opp;
+        }
+      }
+      if (threadIdx.x == 0) {
+        ctl.xb_min[0] = br;
+        ctl.xb_min[1] = bp;
+      }
+    }
+    __syncthreads();
+    const uint64_t tb_r = ctl.xb_min[0], tb_p = ctl.xb_min[1];
+    // every CTA's surviving entries into the leader's ring, one warp-wide atomic per 32 entries
     const uint32_t cap = C * (p.merge_gather == 2 ? L : k);
     Raw* g_raw = reinterpret_cast<Raw*>(ring);
     uint32_t* g_idx = reinterpret_cast<uint32_t*>(ring + align16(cap * sizeof(Raw)));
@@ -536,7 +584,12 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
     const uint32_t gcnt = dsmem_map(smem_addr(&ctl.gather_count), leader);
     for (uint32_t base = 0; base < count; base += NT) {
       const uint32_t e = base + threadIdx.x;
-      const bool valid = e < count;
+      bool valid = e < count;
+      if (valid) {
+        const uint64_t r = (uint64_t)TR::rank(list_raw[e], dirmask);
+        const uint64_t pi = pref_index(list_idx[e], pl);
+        valid = r < tb_r || (r == tb_r && pi <= tb_p);
+      }
       const uint32_t bal = __ballot_sync(kFull, valid);
       if (bal) {
         uint32_t wb = 0;
@@ -571,14 +624,16 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
       for (uint32_t e = threadIdx.x; e < count; e += NT) {
         const Rank r = TR::rank(list_raw[e], dirmask);
         if ((r & sel.mask) == sel.prefix)
-          atomicAdd(&ctl.hist[0][(uint32_t)(r >> shift) & (kBuckets - 1)], 1u);
+          atomicAdd(&ctl.hist_m0[(uint32_t)(r >> shift) & (kBuckets - 1)], 1u);
       }
       __syncthreads();
-      if (rank != leader && threadIdx.x < kBuckets) {
-        const uint32_t v = ctl.hist[0][threadIdx.x];
-        if (v)
-          dsmem_red_add(merged_addr + 4u * threadIdx.x, v);
-        ctl.hist[0][threadIdx.x] = 0;
+      if (rank != leader) {
+        for (uint32_t i = threadIdx.x; i < (uint32_t)kBuckets; i += NT) {
+          const uint32_t v = ctl.hist_m0[i];
+          if (v)
+            dsmem_red_add(merged_addr + 4u * i, v);
+          ctl.hist_m0[i] = 0;
+        }
       }
       cluster_sync(); // every fold has landed in the leader
       if (rank == leader && threadIdx.x < 32) {
@@ -586,9 +641,9 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const uint32_t b = 8 * threadIdx.x + i;
-          h[i] = ctl.hist_merged[b] + ctl.hist[0][b];
+          h[i] = ctl.hist_merged[b] + ctl.hist_m0[b];
           ctl.hist_merged[b] = 0;
-          ctl.hist[0][b] = 0;
+          ctl.hist_m0[b] = 0;
         }
         find_bucket(h, krem, ctl.res);
       }
@@ -643,7 +698,7 @@ __global__ void __launch_bounds__(NT, 2) stream_topk_kernel(const KernelParams p
   {
     CandBuf cb = cbuf;
     cb.n = ~0u;
-    select_ties<TR, NT>(ctl, lsrc, quota, dirmask, pl, sel, cb);
+    select_ties<TR, NT>(ctl, sel_pass, lsrc, quota, dirmask, pl, sel, cb);
   }
   const bool take_ties = quota > 0;
   auto classify = [&](uint32_t, Raw, uint32_t ki, Rank rk) {
