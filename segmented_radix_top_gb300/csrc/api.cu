@@ -77,9 +77,13 @@ struct Plan {
   uint32_t list_cap;
   uint32_t ring_bytes;
   int merge_gather;
+  int64_t waves; // waves of resident CTAs (or clusters) over all segments
 };
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Largest C * k for which the cluster gathers local top-k lists into the leader.
+constexpr uint32_t kGatherMaxItems = 2048;
 
 // Candidate-list room beyond k: keys accepted after a selection before the
 // list overflows and the next selection (over the list and the chunk being
@@ -100,9 +104,12 @@ Plan size_plan(const KeyOps& ops, int32_t k, int cluster)
   pl.merge_gather = 0;
   if (cluster > 1) {
     // 2: every CTA's whole list fits in the leader (no local trims);
-    // 1: every CTA's local top-k fits; 0: histogram merge through DSMEM
+    // 1: every CTA's local top-k fits and the leader's selection over them
+    // stays short; 0: histogram merge through DSMEM (measured faster than a
+    // gather of more than kGatherMaxItems entries, whose serial selection
+    // and tie resolution in the leader dominate)
     auto gather_need = [&](uint32_t cap) { return align16(cap * kb) + align16(cap * 4u) + sort_need; };
-    if (gather_need((uint32_t)cluster * uk) <= stream_ring)
+    if (gather_need((uint32_t)cluster * uk) <= stream_ring && (uint32_t)cluster * uk <= kGatherMaxItems)
       pl.merge_gather = 1;
     need = pl.merge_gather ? gather_need((uint32_t)cluster * (pl.merge_gather == 2 ? pl.list_cap : uk))
                            : align16(uk * kb) + align16(uk * 4u) + sort_need;
@@ -141,6 +148,7 @@ cudaError_t choose_plan(const KeyOps& ops, int64_t num_segments, int64_t max_len
     if (!have || waves <= best_waves) {
       have = true;
       best_waves = waves;
+      pl.waves = waves;
       *out = pl;
     }
   }
@@ -176,6 +184,7 @@ cudaError_t get_plan(int dtype, const KeyOps& ops, int64_t num_segments, int64_t
     pl = size_plan(ops, k, forced_width);
     int resident = 0;
     e = ops.occupancy(pl.shape, &resident);
+    pl.waves = resident > 0 ? (num_segments + resident - 1) / resident : 0;
     if (e != cudaSuccess || resident <= 0) {
       (void)cudaGetLastError();
       *unsupported = true;
@@ -313,6 +322,10 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
   p.k = k;
   p.list_cap = pl.list_cap;
   p.merge_gather = pl.merge_gather;
+  // Speculative-bound sample: with one wave the slowest CTA sets the time, so
+  // a larger sample (a steadier bound); with many waves the mean matters, so
+  // a smaller one (less selection work per segment).
+  p.spec_keys = pl.waves <= 1 ? 2048u : 1024u;
   p.ring_stages = kStages;
   p.ring_bytes = pl.ring_bytes;
   p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;

@@ -677,16 +677,35 @@ __device__ __noinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t pa
 {
   using Rank = typename TR::Rank;
   constexpr Rank kWorst = (TR::kRankBits == 64) ? ~(Rank)0 : (Rank)(((uint64_t)1 << TR::kRankBits) - 1);
-  const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, pass, src.size(), nullptr, 0u, mm, mm,
-                                                               8u * mm + 64u, cb, [&](uint32_t e, Rank& key) {
-                                                                 key = TR::rank(src.key(e), dirmask);
-                                                                 return true;
-                                                               });
-  const Rank edge = rr.prefix | (~rr.mask & kWorst);
-  const uint32_t total = mm - rr.krem + rr.cnt;
-  if (!rr.stopped || edge == kWorst || total > cap)
+  Selection<Rank> s;
+  Rank edge;
+  uint32_t total;
+  bool ok;
+  if constexpr (TR::kRankBits == 64) {
+    // 64-bit ranks: the high word is resolution enough for a first bound
+    const Radix<uint32_t> rr = radix_select<uint32_t, 32, NT>(ctl, pass, src.size(), nullptr, 0u, mm, mm,
+                                                              8u * mm + 64u, cb, [&](uint32_t e, uint32_t& key) {
+                                                                key = (uint32_t)(TR::rank(src.key(e), dirmask) >> 32);
+                                                                return true;
+                                                              });
+    const uint32_t edge_hi = rr.prefix | ~rr.mask;
+    edge = ((Rank)edge_hi << 32) | 0xffffffffull;
+    total = mm - rr.krem + rr.cnt;
+    ok = rr.stopped;
+    s = Selection<Rank>{(Rank)rr.prefix << 32, (Rank)rr.mask << 32, 0u, 0u, total};
+  } else {
+    const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, pass, src.size(), nullptr, 0u, mm, mm,
+                                                                 8u * mm + 64u, cb, [&](uint32_t e, Rank& key) {
+                                                                   key = TR::rank(src.key(e), dirmask);
+                                                                   return true;
+                                                                 });
+    edge = rr.prefix | (~rr.mask & kWorst);
+    total = mm - rr.krem + rr.cnt;
+    ok = rr.stopped;
+    s = Selection<Rank>{rr.prefix, rr.mask, 0u, 0u, total}; // the whole boundary bucket
+  }
+  if (!ok || edge == kWorst || total > cap)
     return Spec<Rank>{false, (Rank)0, 0u, pass};
-  const Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u, total}; // the whole boundary bucket
   const Kept<Rank> kp = select_into<TR, NT>(ctl, pass, src, s, dst_raw, dst_idx, cap, dirmask, false);
   return Spec<Rank>{true, edge, kp.n, pass};
 }

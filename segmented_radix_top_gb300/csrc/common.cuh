@@ -304,19 +304,23 @@ struct KeyTraits<KeyKind::F64> {
   {
     return FloatRank<uint64_t, 64>::t_inv(r ^ dirmask);
   }
-  // the exact high 32 bits of a key's rank, from its two words
-  __device__ __forceinline__ static uint32_t rank_hi(uint32_t lo, uint32_t hi, uint32_t dm_hi)
+  // The high word of a double as a signed integer in the double's own order
+  // (sign-magnitude to two's complement); -0.0 lands one below +0.0, which
+  // only widens the superset test below.
+  __device__ __forceinline__ static int32_t order_hi(uint32_t hi)
   {
-    if (hi == 0x80000000u && lo == 0u)
-      hi = 0u; // -0.0
-    return (hi ^ ((hi & 0x80000000u) ? 0xffffffffu : 0x80000000u)) ^ dm_hi;
+    const int32_t x = (int32_t)hi;
+    return x ^ (int32_t)((uint32_t)(x >> 31) >> 1);
   }
   __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
   {
-    // rank < tau implies rank_hi <= tau_hi: a superset test on one word
-    const uint32_t dm_hi = is_max ? 0xffffffffu : 0u;
-    const uint32_t th = (uint32_t)(b.tau >> 32);
-    return (rank_hi(v.x, v.y, dm_hi) <= th) | (rank_hi(v.z, v.w, dm_hi) <= th);
+    // a key ranking below the bound is, as a number, at least (max) or at
+    // most (min) the bound key, so its high word compares likewise
+    const int32_t ob = order_hi((uint32_t)(b.raw >> 32));
+    const int32_t o0 = order_hi(v.y), o1 = order_hi(v.w);
+    if (is_max)
+      return (o0 >= ob) | (o1 >= ob);
+    return (o0 <= ob) | (o1 <= ob);
   }
 };
 

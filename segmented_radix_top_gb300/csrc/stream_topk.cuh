@@ -58,6 +58,7 @@ struct KernelParams {
   int32_t sorted;        // write the selected items in stable sorted order
   int32_t merge_gather;  // cluster merge: 2 gather whole lists, 1 gather local top-k, 0 histograms
   int32_t flag_overlong; // report segments longer than n_hi
+  uint32_t spec_keys;    // sample size of the speculative first bound
 };
 
 // Host and device agree on the dynamic shared-memory layout.
@@ -66,7 +67,7 @@ __host__ __device__ inline uint32_t list_bytes(uint32_t cap, uint32_t key_bytes)
 {
   return align16(cap * key_bytes) + cap * 4u;
 }
-// Keys of the first chunk used to form the first bound.
+// Least sample of an exact first bound (keys of the first chunk).
 constexpr uint32_t kBootKeys = 2048;
 // Candidate positions kept by a selection between its passes.
 constexpr uint32_t kCandCap = 4096;
@@ -427,21 +428,22 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) stream_topk_kernel(const Kerne
           count += nkeys;
         } else {
           // the first bound, from the list and the most preferred keys of this
-          // chunk (enough to pass k, at least kBootKeys); the rest of the chunk
-          // comes later in preference order and is offered against it
-          const uint32_t want = max(k + 1 - count, (uint32_t)kBootKeys);
-          const uint32_t nb = min(nv, (want + VK - 1) / VK);
-          const uint32_t b0 = fwd ? 0u : nv - nb; // first vector of the sample
-          const uint32_t ns = count + nb * VK;
+          // chunk (the rest of the chunk comes later in preference order and
+          // is offered against it): speculative from p.spec_keys of them, else
+          // the exact k best of enough to pass k, at least kBootKeys
+          uint32_t nb = 0;
           bool done = false;
           if (allow_spec) {
+            const uint32_t nbs = min(nv, (p.spec_keys + VK - 1) / VK);
+            const uint32_t ns = count + nbs * VK;
             const float mu = (float)k * (float)ns / (float)n_slice;
             const uint32_t mm = (uint32_t)ceilf(mu + 4.0f * sqrtf(mu) + 3.0f);
             if (mm < k && mm < ns) {
+              const uint32_t b0 = fwd ? 0u : nv - nbs;
               const Spec<Rank> sp =
                 spec_into<TR, NT>(ctl, sel_pass,
                                   Src<Raw>{list_raw, list_idx, count, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK,
-                                           nb * VK},
+                                           nbs * VK},
                                   spare_raw, spare_idx, mm, L, dirmask, cbuf);
               sel_pass = sp.pass;
               if (sp.ok) {
@@ -449,11 +451,16 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) stream_topk_kernel(const Kerne
                 set_bound(sp.edge + 1, sp.n); // accept rank <= edge
                 spec_used = true;
                 done = true;
+                nb = nbs;
               }
             }
           }
-          if (!done)
+          if (!done) {
+            const uint32_t want = max(k + 1 - count, (uint32_t)kBootKeys);
+            nb = min(nv, (want + VK - 1) / VK);
+            const uint32_t b0 = fwd ? 0u : nv - nb;
             select_union(stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nb * VK, trim_slack);
+          }
           if (nb < nv)
             process_vectors(stage, fwd ? nb : 0u, fwd ? nv : nv - nb, idx0);
         }

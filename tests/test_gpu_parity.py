@@ -145,3 +145,22 @@ def test_repeat_runs_identical():
     for _ in range(2):
         b = run_gpu(wl)
         assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f64", "f16", "u32"])
+def test_many_single_cta_segments(dtype):
+    """Several waves of single-CTA segments (more segments than resident
+    CTAs), the sample size of the speculative bound chosen for many waves.
+    Lengths mix empty, tiny, n <= k and multi-chunk segments at unaligned
+    starts."""
+    g = np.random.Generator(np.random.PCG64(77))
+    lengths = np.where(g.random(1400) < 0.1, 0, g.integers(1, 20000, size=1400))
+    lengths[::37] = g.integers(20000, 60000, size=len(lengths[::37]))
+    for i, (k, tie, ordering, direction) in enumerate([
+            (1, "prefer_smaller_index", "stable_sorted", "max"),
+            (50, "prefer_larger_index", "unsorted", "min"),
+            (300, "prefer_smaller_index", "sorted", "max"),
+            (2048, "prefer_larger_index", "stable_sorted", "min")]):
+        wl = W.random_workload(900 + i, dtype, lengths, k, direction, "gpu_to_gpu", tie, ordering,
+                               pairs=(i % 2 == 0), distinct=(40 if i == 1 else None), lead=1 + i)
+        check_workload(wl, cluster_width=1, where="many segments %s k=%d %s %s" % (dtype, k, tie, ordering))
