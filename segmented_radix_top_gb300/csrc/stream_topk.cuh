@@ -496,10 +496,11 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) stream_topk_kernel(const Kerne
   }
 
   // local top-k of this CTA's slice, for clusters that gather top-k lists
-  // or merge histograms (a lone CTA, or a cluster that gathers whole lists,
-  // selects once when writing the output)
+  // (a lone CTA selects once when writing the output; the histogram merge
+  // works on whole lists: each holds its slice's top-k and, at the boundary
+  // rank, a preference-order prefix of the slice's ties)
   __syncthreads();
-  if (count > k && C > 1 && p.merge_gather != 2)
+  if (count > k && C > 1 && p.merge_gather == 1)
     trim_list(0u);
 
   Raw* out_keys = reinterpret_cast<Raw*>(p.out_keys) + seg * (int64_t)k;
