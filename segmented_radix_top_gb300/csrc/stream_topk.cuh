@@ -67,7 +67,8 @@ __host__ __device__ inline uint32_t list_bytes(uint32_t cap, uint32_t key_bytes)
 {
   return align16(cap * key_bytes) + cap * 4u;
 }
-// Least sample of an exact first bound (keys of the first chunk).
+// Least sample of an exact first bound (keys of the first chunk; at least
+// four times k are taken).
 constexpr uint32_t kBootKeys = 2048;
 // Candidate positions kept by a selection between its passes.
 constexpr uint32_t kCandCap = 4096;
@@ -456,7 +457,10 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) stream_topk_kernel(const Kerne
             }
           }
           if (!done) {
-            const uint32_t want = max(k + 1 - count, (uint32_t)kBootKeys);
+            // several times k, so that the sample's k-th key sits where the
+            // slice's will (with fewer, a tie block cut short by sampling
+            // noise leaves the bound below the ties and lets them all in)
+            const uint32_t want = max(k + 1 - count, max(4u * k, (uint32_t)kBootKeys));
             nb = min(nv, (want + VK - 1) / VK);
             const uint32_t b0 = fwd ? 0u : nv - nb;
             select_union(stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nb * VK, trim_slack);
