@@ -264,11 +264,11 @@ __device__ __forceinline__ void finish_by_count(Key* stage, uint32_t* nfin, cons
 // selection unresolved (stopped = false), for callers that only want a
 // cheap answer.
 //
-// Work saving: pass 0 also records the AND / OR of every candidate key and
-// pass 1 those of the remaining candidates, together with their positions
-// in `cb` when they fit; later passes then visit only those positions, a
-// digit on which all remaining candidates agree is folded without a pass,
-// and at most kFinishMax boundary candidates are resolved by counting.
+// Work saving: every pass also records the AND / OR of the candidate keys
+// it visits, and pass 1 their positions in `cb` when they fit; later passes
+// then visit only those positions, a digit on which all candidates of the
+// previous pass agree is folded without a pass, and at most kFinishMax
+// boundary candidates are resolved by counting.
 // Each pass takes one barrier: every warp finds the bucket itself. `pass`
 // is the block's pass counter (see PassSlot). Requires at least kk
 // candidates. Block-wide.
@@ -296,7 +296,7 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t& pass, uint32_t count, co
     }
     PassSlot& sl = ctl.slot[pass % 3];
     uint32_t* h = sl.hist;
-    const bool rec = p <= 1; // record AND / OR
+    const bool rec = true; // record AND / OR (every pass: a digit its candidates share is folded next)
     const bool collect = p == 1 && can_compact;
     const uint32_t n_visit = compacted ? ncand : span;
     Key ta = ~(Key)0, to = (Key)0;
@@ -429,6 +429,60 @@ __device__ void select_ties(Ctrl& ctl, uint32_t& pass, const Src<typename TR::Ra
   s.imask = ri.mask;
 }
 
+// Boundary ties when every entry of `src` is a ring key (no list entries):
+// position order is source-index order, so the q preferred ties are the
+// first q (prefer_smaller) or last q (prefer_larger) ties by position. Each
+// thread counts the ties in its run of consecutive entries, a block scan
+// over the counts gives every run's first tie number, and the thread
+// holding the q-th preferred tie publishes its preference index, which
+// becomes the tie threshold ("Implement Segmented TopK using
+// Thread-Block-Clusters", section 5: ties taken in index order by prefix
+// scans). Block-wide.
+template <class TR, int NT>
+__device__ __forceinline__ void select_ties_ordered(Ctrl& ctl, const Src<typename TR::Raw>& src, uint32_t q,
+                                                 typename TR::Rank dirmask, bool prefer_larger,
+                                                 Selection<typename TR::Rank>& s)
+{
+  using Rank = typename TR::Rank;
+  const Rank prefix = s.prefix, mask = s.mask;
+  const uint32_t n = src.ext_count;
+  const uint32_t per = (n + NT - 1) / NT;
+  const uint32_t e0 = min(n, threadIdx.x * per), e1 = min(n, e0 + per);
+  uint32_t c = 0;
+  for (uint32_t e = e0; e < e1; ++e)
+    c += (TR::rank(src.ext_raw[e], dirmask) & mask) == prefix ? 1u : 0u;
+  // block exclusive scan of c over threads in position order
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_inclusive_sum(c);
+  if (lane == 31)
+    ctl.red[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0, total = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    const uint32_t t = (uint32_t)ctl.red[w];
+    before += (uint32_t)w < warp ? t : 0u;
+    total += t;
+  }
+  const uint32_t excl = before + incl - c;
+  // 0-based position (ascending) of the q-th preferred tie
+  const uint32_t target = prefer_larger ? total - q : q - 1;
+  if (target >= excl && target < excl + c) {
+    uint32_t r = excl;
+    for (uint32_t e = e0; e < e1; ++e) {
+      if ((TR::rank(src.ext_raw[e], dirmask) & mask) == prefix) {
+        if (r == target)
+          ctl.res[0] = pref_index(src.ext_idx0 + e, prefer_larger);
+        ++r;
+      }
+    }
+  }
+  __syncthreads();
+  s.iprefix = ctl.res[0];
+  s.imask = ~0u;
+  __syncthreads(); // ctl.red and ctl.res are free again
+}
+
 // The kk best of the entries of `src` (size > kk > 0) in one CTA -- or,
 // with slack > 0, between kk and kk + slack entries that include them: a
 // radix selection on the rank code, then, if more boundary entries tie than
@@ -447,6 +501,8 @@ __device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, uint32_t& pass, 
   Selection<Rank> s{rr.prefix, rr.mask, 0u, 0u, kk};
   if (rr.stopped) // the whole boundary bucket is taken
     s.n = kk - rr.krem + rr.cnt;
+  else if (src.count == 0) // every rank digit resolved, more than krem ties, ring keys only
+    select_ties_ordered<TR, NT>(ctl, src, rr.krem, dirmask, prefer_larger, s);
   else // every rank digit resolved and more than krem entries share the boundary rank
     select_ties<TR, NT>(ctl, pass, src, rr.krem, dirmask, prefer_larger, s, cb);
   return s;
