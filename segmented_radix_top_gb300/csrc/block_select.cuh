@@ -699,7 +699,7 @@ __device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, uint32
 // keys (which come after every kept one in preference order) are accepted
 // only below it.
 template <class TR, int NT>
-__device__ __noinline__ Kept<typename TR::Rank> trim_into(Ctrl& ctl, uint32_t pass, const Src<typename TR::Raw> src,
+__device__ __forceinline__ Kept<typename TR::Rank> trim_into(Ctrl& ctl, uint32_t pass, const Src<typename TR::Raw> src,
                                                           typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t kk,
                                                           uint32_t slack, typename TR::Rank dirmask,
                                                           bool prefer_larger, CandBuf cb)
@@ -727,7 +727,7 @@ struct Spec {
   uint32_t pass;
 };
 template <class TR, int NT>
-__device__ __noinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t pass, const Src<typename TR::Raw> src,
+__device__ __forceinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t pass, const Src<typename TR::Raw> src,
                                                           typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t mm,
                                                           uint32_t cap, typename TR::Rank dirmask, CandBuf cb)
 {
