@@ -887,7 +887,7 @@ __host__ __device__ inline uint32_t finalize_scratch_bytes(uint32_t n) { return 
 // index). `scratch` holds finalize_scratch_bytes(n) bytes (shared memory);
 // the entries must be visible to the whole block.
 template <class TR, int NT>
-__device__ __noinline__ void finalize_small(const typename TR::Raw* raw, const uint32_t* idx, uint32_t n, uint32_t k,
+__device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, const uint32_t* idx, uint32_t n, uint32_t k,
                                             typename TR::Rank dirmask, bool prefer_larger, bool sorted,
                                             unsigned char* scratch, typename TR::Raw* out_keys, int32_t* out_values,
                                             const int32_t* values)
@@ -948,7 +948,7 @@ __device__ __noinline__ void finalize_small(const typename TR::Raw* raw, const u
 // slots of one segment. `scratch` must hold sort_scratch_bytes(m) bytes and
 // the items must be visible to the whole block.
 template <class TR, int NT>
-__device__ __noinline__ void sort_and_write(const typename TR::Raw* raw, const uint32_t* idx, uint32_t m,
+__device__ __forceinline__ void sort_and_write(const typename TR::Raw* raw, const uint32_t* idx, uint32_t m,
                                             typename TR::Rank dirmask, unsigned char* scratch,
                                             typename TR::Raw* out_keys, int32_t* out_values,
                                             const int32_t* values)
