@@ -82,6 +82,10 @@ struct Plan {
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
+// Margin of the speculative bound with several waves of segments.
+constexpr float kSpecZ = 2.0f;
+constexpr float kSpecC = 1.0f;
+
 // Largest C * k for which the cluster gathers local top-k lists into the leader.
 constexpr uint32_t kGatherMaxItems = 2048;
 
@@ -326,6 +330,12 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
   // a larger sample (a steadier bound); with many waves the mean matters, so
   // a smaller one (less selection work per segment).
   p.spec_keys = pl.waves <= 1 ? 2048u : 1024u;
+  // Its margin, in standard deviations of the sample's share of the k best:
+  // a slice whose bound proves too tight is read twice, which with one wave
+  // sets the kernel's time (wide margin) and with many waves is averaged out
+  // (narrower margin, shorter lists).
+  p.spec_z = pl.waves <= 1 ? 4.0f : kSpecZ;
+  p.spec_c = pl.waves <= 1 ? 3.0f : kSpecC;
   p.ring_stages = kStages;
   p.ring_bytes = pl.ring_bytes;
   p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;

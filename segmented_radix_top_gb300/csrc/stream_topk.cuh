@@ -59,6 +59,8 @@ struct KernelParams {
   int32_t merge_gather;  // cluster merge: 2 gather whole lists, 1 gather local top-k, 0 histograms
   int32_t flag_overlong; // report segments longer than n_hi
   uint32_t spec_keys;    // sample size of the speculative first bound
+  float spec_z;          // its margin: mu + spec_z * sqrt(mu) + spec_c sample keys are kept
+  float spec_c;
 };
 
 // Host and device agree on the dynamic shared-memory layout.
@@ -438,7 +440,7 @@ __global__ void __launch_bounds__(NT, kCtasPerSm) stream_topk_kernel(const Kerne
             const uint32_t nbs = min(nv, (p.spec_keys + VK - 1) / VK);
             const uint32_t ns = count + nbs * VK;
             const float mu = (float)k * (float)ns / (float)n_slice;
-            const uint32_t mm = (uint32_t)ceilf(mu + 4.0f * sqrtf(mu) + 3.0f);
+            const uint32_t mm = (uint32_t)ceilf(mu + p.spec_z * sqrtf(mu) + p.spec_c);
             if (mm < k && mm < ns) {
               const uint32_t b0 = fwd ? 0u : nv - nbs;
               const Spec<Rank> sp =
