@@ -94,15 +94,19 @@ constexpr uint32_t kGatherMaxItems = 2048;
 // read) tightens the bound.
 uint32_t list_slack(uint32_t k) { return std::max(1024u, k / 2); }
 
-// Shared-memory sizing for a given k and cluster width. The ring doubles as
-// sort scratch and, in a cluster leader, as gather space.
-Plan size_plan(const KeyOps& ops, int32_t k, int cluster)
+// Ring-stage and candidate-buffer bytes of a kernel profile.
+uint32_t profile_chunk_bytes(int profile) { return profile == 0 ? ProfileLong::kChunkBytes : ProfileMany::kChunkBytes; }
+uint32_t profile_cand_bytes(int profile) { return profile == 0 ? ProfileLong::kCandBytes : ProfileMany::kCandBytes; }
+
+// Shared-memory sizing for a given k, cluster width and kernel profile. The
+// ring doubles as sort scratch and, in a cluster leader, as gather space.
+Plan size_plan(const KeyOps& ops, int32_t k, int cluster, int profile)
 {
   Plan pl;
   const uint32_t kb = (uint32_t)ops.key_bytes;
   const uint32_t uk = (uint32_t)k;
   pl.list_cap = align_up(uk + list_slack(uk), 32);
-  const uint32_t stream_ring = kStages * kChunkBytes;
+  const uint32_t stream_ring = kStages * profile_chunk_bytes(profile);
   const uint32_t sort_need = std::max(sort_scratch_bytes(uk, ops.rank_bits), finalize_scratch_bytes(kCountMax));
   uint32_t need = sort_need;
   pl.merge_gather = 0;
@@ -121,7 +125,8 @@ Plan size_plan(const KeyOps& ops, int32_t k, int cluster)
   pl.ring_bytes = align_up(std::max(stream_ring, need), 128);
   pl.shape.threads = kThreads;
   pl.shape.cluster = cluster;
-  pl.shape.smem = kCtrlBytes + pl.ring_bytes + 2 * list_bytes(pl.list_cap, kb) + kCandBytes;
+  pl.shape.profile = profile;
+  pl.shape.smem = kCtrlBytes + pl.ring_bytes + 2 * list_bytes(pl.list_cap, kb) + profile_cand_bytes(profile);
   return pl;
 }
 
@@ -139,9 +144,9 @@ cudaError_t choose_plan(const KeyOps& ops, int64_t num_segments, int64_t max_len
   for (int c : widths) {
     if (c > 1 && max_len < (int64_t)c * kMinSliceKeys)
       break;
-    Plan pl = size_plan(ops, k, c);
+    Plan pl = size_plan(ops, k, c, 0);
     int resident = 0;
-    cudaError_t e = ops.occupancy(pl.shape, &resident);
+    cudaError_t e = ops.occupancy[0](pl.shape, &resident);
     if (e != cudaSuccess) {
       (void)cudaGetLastError(); // an unlaunchable width is skipped, not an error
       continue;
@@ -185,9 +190,9 @@ cudaError_t get_plan(int dtype, const KeyOps& ops, int64_t num_segments, int64_t
   }
   Plan pl;
   if (forced_width > 0) {
-    pl = size_plan(ops, k, forced_width);
+    pl = size_plan(ops, k, forced_width, 0);
     int resident = 0;
-    e = ops.occupancy(pl.shape, &resident);
+    e = ops.occupancy[0](pl.shape, &resident);
     pl.waves = resident > 0 ? (num_segments + resident - 1) / resident : 0;
     if (e != cudaSuccess || resident <= 0) {
       (void)cudaGetLastError();
@@ -198,6 +203,19 @@ cudaError_t get_plan(int dtype, const KeyOps& ops, int64_t num_segments, int64_t
     e = choose_plan(ops, num_segments, max_len, k, &pl);
     if (e != cudaSuccess)
       return e;
+  }
+  if (pl.shape.cluster == 1 && pl.waves > 1) {
+    // several waves of single CTAs: the profile with more CTAs per SM, so
+    // that one CTA's selections overlap the others' streams
+    Plan pm = size_plan(ops, k, 1, 1);
+    int resident = 0;
+    e = ops.occupancy[1](pm.shape, &resident);
+    if (e == cudaSuccess && resident > 0) {
+      pm.waves = (num_segments + resident - 1) / resident;
+      pl = pm;
+    } else {
+      (void)cudaGetLastError(); // keep the first profile
+    }
   }
   std::lock_guard<std::mutex> lk(g_plan_mu);
   if (g_plans.size() > 4096)
@@ -341,7 +359,7 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
   p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;
   p.sorted = (ordering != SEGTOPK_UNSORTED) ? 1 : 0;
   p.flag_overlong = 1;
-  e = ops.launch(p, pl.shape, st);
+  e = ops.launch[pl.shape.profile](p, pl.shape, st);
   if (e != cudaSuccess)
     return cuda_fail(e);
   t_last_launch_count = 1;

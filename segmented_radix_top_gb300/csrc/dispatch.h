@@ -13,16 +13,19 @@ struct LaunchShape {
   int threads;        // CTA size
   int cluster;        // CTAs per segment (1 = plain launch)
   uint32_t smem;      // dynamic shared memory bytes
+  int profile;        // kernel profile: 0 long segments, 1 many single-CTA segments
 };
+
+constexpr int kProfiles = 2;
 
 // Entry points every key-type translation unit provides.
 struct KeyOps {
   int key_bytes;
   int rank_bits;
-  // Launch the segment kernel over all num_segments segments.
-  cudaError_t (*launch)(const KernelParams& p, const LaunchShape& s, cudaStream_t stream);
+  // Launch the segment kernel (profile s.profile) over all num_segments segments.
+  cudaError_t (*launch[kProfiles])(const KernelParams& p, const LaunchShape& s, cudaStream_t stream);
   // Resident clusters (cluster > 1) or resident CTAs (cluster == 1) per GPU.
-  cudaError_t (*occupancy)(const LaunchShape& s, int* resident);
+  cudaError_t (*occupancy[kProfiles])(const LaunchShape& s, int* resident);
   // Read and clear this translation unit's device error word (synchronous).
   cudaError_t (*read_error)(uint32_t* word);
 };

@@ -6,14 +6,14 @@
 
 namespace segtopk {
 
-template <KeyKind KK, int NT>
+template <KeyKind KK, int NT, class PR>
 struct StreamLauncher {
   static cudaError_t prepare(uint32_t smem, int cluster)
   {
     // Raise the dynamic shared-memory opt-in lazily, only as far as needed.
     static uint32_t granted = 0;
     static bool nonportable = false;
-    auto fn = stream_topk_kernel<KK, NT>;
+    auto fn = stream_topk_kernel<KK, NT, PR>;
     if (smem > granted) {
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess)
@@ -56,7 +56,7 @@ struct StreamLauncher {
     cudaLaunchAttribute attr[1];
     config(s, p.num_segments, cfg, attr);
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, stream_topk_kernel<KK, NT>, p);
+    return cudaLaunchKernelEx(&cfg, stream_topk_kernel<KK, NT, PR>, p);
   }
 
   static cudaError_t occupancy(const LaunchShape& s, int* resident)
@@ -66,7 +66,7 @@ struct StreamLauncher {
       return e;
     if (s.cluster <= 1) {
       int per_sm = 0, dev = 0, sms = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_topk_kernel<KK, NT>, NT, s.smem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stream_topk_kernel<KK, NT, PR>, NT, s.smem);
       if (e != cudaSuccess)
         return e;
       e = cudaGetDevice(&dev);
@@ -79,7 +79,7 @@ struct StreamLauncher {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     config(s, s.cluster, cfg, attr);
-    return cudaOccupancyMaxActiveClusters(resident, stream_topk_kernel<KK, NT>, &cfg);
+    return cudaOccupancyMaxActiveClusters(resident, stream_topk_kernel<KK, NT, PR>, &cfg);
   }
 };
 
@@ -98,9 +98,13 @@ inline cudaError_t read_and_clear(uint32_t* word)
   namespace segtopk {                                                                              \
   const KeyOps& key_ops_##NAME()                                                                   \
   {                                                                                                \
-    static const KeyOps ops = {(int)sizeof(KeyTraits<KIND>::Raw), KeyTraits<KIND>::kRankBits,     \
-                               &StreamLauncher<KIND, kCtaThreads>::launch,                         \
-                               &StreamLauncher<KIND, kCtaThreads>::occupancy, &read_and_clear};    \
+    static const KeyOps ops = {(int)sizeof(KeyTraits<KIND>::Raw),                                 \
+                               KeyTraits<KIND>::kRankBits,                                         \
+                               {&StreamLauncher<KIND, kCtaThreads, ProfileLong>::launch,           \
+                                &StreamLauncher<KIND, kCtaThreads, ProfileMany>::launch},          \
+                               {&StreamLauncher<KIND, kCtaThreads, ProfileLong>::occupancy,        \
+                                &StreamLauncher<KIND, kCtaThreads, ProfileMany>::occupancy},       \
+                               &read_and_clear};                                                   \
     return ops;                                                                                    \
   }                                                                                                \
   }

@@ -33,12 +33,26 @@
 
 namespace segtopk {
 
-// Threads per CTA, CTAs an SM is sized for, and 16-byte vectors a thread
-// filters per ring stage (one stage = kCtaThreads * kVecPerThread vectors).
+// Threads per CTA.
 constexpr int kCtaThreads = 256;
-constexpr int kCtasPerSm = 2;
-constexpr int kVecPerThread = 8;
-constexpr uint32_t kChunkBytes = 16u * (uint32_t)kVecPerThread * (uint32_t)kCtaThreads;
+
+// A kernel profile: CTAs an SM is sized for, 16-byte vectors a thread filters
+// per ring stage (a stage holds kCtaThreads * VEC_PER_THREAD vectors), and
+// the capacity of the selection's candidate-position buffer.
+template <int CTAS_PER_SM, int VEC_PER_THREAD, uint32_t CAND_CAP>
+struct CtaProfile {
+  static constexpr int kCtasPerSm = CTAS_PER_SM;
+  static constexpr int kVecPerThread = VEC_PER_THREAD;
+  static constexpr uint32_t kChunkBytes = 16u * (uint32_t)VEC_PER_THREAD * (uint32_t)kCtaThreads;
+  static constexpr uint32_t kCandCap = CAND_CAP;
+  static constexpr uint32_t kCandBytes = CAND_CAP * 2u;
+};
+// Long segments served by one wave of CTAs or clusters: two CTAs per SM,
+// 32 KiB stages (fewer, larger chunks per segment).
+using ProfileLong = CtaProfile<2, 8, 4096>;
+// Several waves of single-CTA segments: three CTAs per SM, 16 KiB stages,
+// so that one CTA's selections overlap the others' streams.
+using ProfileMany = CtaProfile<3, 4, 2048>;
 
 struct KernelParams {
   const void* keys;
@@ -72,17 +86,16 @@ __host__ __device__ inline uint32_t list_bytes(uint32_t cap, uint32_t key_bytes)
 // Least sample of an exact first bound (keys of the first chunk; at least
 // four times k are taken).
 constexpr uint32_t kBootKeys = 2048;
-// Candidate positions kept by a selection between its passes.
-constexpr uint32_t kCandCap = 4096;
-constexpr uint32_t kCandBytes = kCandCap * 2u;
 
-template <KeyKind KK, int NT>
-__global__ void __launch_bounds__(NT, kCtasPerSm) stream_topk_kernel(const KernelParams p)
+template <KeyKind KK, int NT, class PR>
+__global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const KernelParams p)
 {
   using TR = KeyTraits<KK>;
   using Raw = typename TR::Raw;
   using Rank = typename TR::Rank;
   constexpr int VK = 16 / (int)sizeof(Raw);     // keys per 16-byte vector
+  constexpr uint32_t kChunkBytes = PR::kChunkBytes;
+  constexpr uint32_t kCandCap = PR::kCandCap; // candidate positions a selection keeps between passes
   constexpr int U = (int)kChunkBytes / 16 / NT; // vectors per thread per chunk
   constexpr uint32_t kChunkVec = kChunkBytes / 16;
   static_assert(U >= 1 && U <= 8, "chunk / thread configuration");
