@@ -86,6 +86,8 @@ uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 constexpr float kSpecZ = 2.0f;
 constexpr float kSpecC = 1.0f;
 
+// Largest C * k for which the cluster gathers whole candidate lists.
+constexpr uint32_t kGatherListsMaxItems = 512;
 // Largest C * k for which the cluster gathers local top-k lists into the leader.
 constexpr uint32_t kGatherMaxItems = 2048;
 
@@ -111,13 +113,16 @@ Plan size_plan(const KeyOps& ops, int32_t k, int cluster, int profile)
   uint32_t need = sort_need;
   pl.merge_gather = 0;
   if (cluster > 1) {
-    // 2: every CTA's whole list fits in the leader (no local trims);
-    // 1: every CTA's local top-k fits and the leader's selection over them
-    // stays short; 0: histogram merge through DSMEM (measured faster than a
-    // gather of more than kGatherMaxItems entries, whose serial selection
-    // and tie resolution in the leader dominate)
+    // 2: every CTA's whole list fits in the leader and C * k is small: no
+    // local trims, one selection in the leader; 1: every CTA's local top-k
+    // fits and the leader's selection over them stays short; 0: histogram
+    // merge through DSMEM (measured faster than a gather of more than
+    // kGatherMaxItems entries, whose serial selection and tie resolution in
+    // the leader dominate)
     auto gather_need = [&](uint32_t cap) { return align16(cap * kb) + align16(cap * 4u) + sort_need; };
-    if (gather_need((uint32_t)cluster * uk) <= stream_ring && (uint32_t)cluster * uk <= kGatherMaxItems)
+    if (gather_need((uint32_t)cluster * pl.list_cap) <= stream_ring && (uint32_t)cluster * uk <= kGatherListsMaxItems)
+      pl.merge_gather = 2;
+    else if (gather_need((uint32_t)cluster * uk) <= stream_ring && (uint32_t)cluster * uk <= kGatherMaxItems)
       pl.merge_gather = 1;
     need = pl.merge_gather ? gather_need((uint32_t)cluster * (pl.merge_gather == 2 ? pl.list_cap : uk))
                            : align16(uk * kb) + align16(uk * 4u) + sort_need;
