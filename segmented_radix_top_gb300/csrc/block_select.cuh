@@ -767,19 +767,27 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t
 }
 
 // ---------------------------------------------------------------------------
-// Bitonic sort of up to 2048 selected items by (rank ascending, source index
-// ascending), the stable_sorted order of "Top-K: Determinism, Tie-Breaking,
-// and Output Ordering" (Output ordering table). Keys are 64-bit composites
-// rank<<32 | index for ranks up to 32 bits; 64-bit ranks use a (rank, index)
-// pair. The payload is the item's slot in the source arrays.
+// Sorting the selected items (up to 2048) for sorted output: a bitonic
+// network over registers, warp shuffles and, for the widest strides,
+// shared memory.
 // ---------------------------------------------------------------------------
+// Shared-memory bitonic sort of n2 (a power of two) keys with payloads.
+// Compare-exchange pairs: thread i of a stage takes lo = i + (i & ~(stride-1))
+// and hi = lo + stride. A warp's 32 consecutive i cover one aligned block of
+// 64 elements, so stages with stride <= 32 only exchange inside blocks the
+// warp owns and need only a warp barrier; wider strides take block barriers
+// (10 of the 55 stages of a 1024-element sort).
 template <int NT>
 __device__ void bitonic_sort_u64(uint64_t* key, uint32_t* pay, uint32_t n2)
 {
+  bool warp_phase = false; // the last stage synchronised its warp only
   for (uint32_t size = 2; size <= n2; size <<= 1) {
     for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+      const bool block_stage = stride > 32;
+      if (block_stage && warp_phase)
+        __syncthreads();
       for (uint32_t i = threadIdx.x; i < (n2 >> 1); i += NT) {
-        const uint32_t lo = (i / stride) * 2 * stride + (i % stride);
+        const uint32_t lo = i + (i & ~(stride - 1));
         const uint32_t hi = lo + stride;
         const bool up = (lo & size) == 0;
         const uint64_t a = key[lo], b = key[hi];
@@ -791,18 +799,28 @@ __device__ void bitonic_sort_u64(uint64_t* key, uint32_t* pay, uint32_t n2)
           pay[hi] = t;
         }
       }
-      __syncthreads();
+      if (block_stage)
+        __syncthreads();
+      else
+        __syncwarp();
+      warp_phase = !block_stage;
     }
   }
+  if (warp_phase)
+    __syncthreads();
 }
 
 template <int NT>
 __device__ void bitonic_sort_u128(uint64_t* khi, uint64_t* klo, uint32_t n2)
 {
+  bool warp_phase = false;
   for (uint32_t size = 2; size <= n2; size <<= 1) {
     for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+      const bool block_stage = stride > 32;
+      if (block_stage && warp_phase)
+        __syncthreads();
       for (uint32_t i = threadIdx.x; i < (n2 >> 1); i += NT) {
-        const uint32_t lo = (i / stride) * 2 * stride + (i % stride);
+        const uint32_t lo = i + (i & ~(stride - 1));
         const uint32_t hi = lo + stride;
         const bool up = (lo & size) == 0;
         const uint64_t ah = khi[lo], al = klo[lo], bh = khi[hi], bl = klo[hi];
@@ -814,7 +832,99 @@ __device__ void bitonic_sort_u128(uint64_t* khi, uint64_t* klo, uint32_t n2)
           klo[hi] = al;
         }
       }
-      __syncthreads();
+      if (block_stage)
+        __syncthreads();
+      else
+        __syncwarp();
+      warp_phase = !block_stage;
+    }
+  }
+  if (warp_phase)
+    __syncthreads();
+}
+
+// Threads a block sort spreads its elements over (the CTA size).
+constexpr uint32_t kSortLanes = 256;
+
+// In-thread compare-exchange stage of the register sort (stride S < EPT).
+template <int EPT, int S>
+__device__ __forceinline__ void sort_in_thread(uint64_t (&a)[EPT], uint64_t (&b)[EPT], uint32_t size)
+{
+#pragma unroll
+  for (int r = 0; r < EPT; ++r) {
+    if ((r & S) == 0) {
+      const int r2 = r | S;
+      const uint32_t e = threadIdx.x * (uint32_t)EPT + (uint32_t)r;
+      const bool up = (e & size) == 0;
+      const bool gt = a[r] > a[r2] || (a[r] == a[r2] && b[r] > b[r2]);
+      if (gt == up) {
+        const uint64_t ta = a[r], tb = b[r];
+        a[r] = a[r2];
+        b[r] = b[r2];
+        a[r2] = ta;
+        b[r2] = tb;
+      }
+    }
+  }
+}
+
+// Bitonic sort of EPT * NT elements (a, b), ascending by a then b. Thread t
+// holds elements t*EPT .. t*EPT+EPT-1 in registers: strides below EPT are
+// exchanged inside the thread, strides below 32*EPT between lanes of a warp
+// by shuffles, and wider ones through shared memory (s1, s2: one word each
+// per element) with block barriers -- 6 of the 55 stages for 1024 elements.
+template <int NT, int EPT>
+__device__ __forceinline__ void reg_bitonic_sort(uint64_t (&a)[EPT], uint64_t (&b)[EPT], uint64_t* s1, uint64_t* s2)
+{
+  constexpr uint32_t N = (uint32_t)(EPT * NT);
+  const uint32_t t = threadIdx.x;
+  // fully unrolled: every stride is a constant, so each stage compiles to
+  // straight register, shuffle or shared-memory code
+#pragma unroll
+  for (uint32_t size = 2; size <= N; size <<= 1) {
+#pragma unroll
+    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride < (uint32_t)EPT) {
+        if (stride == 4)
+          sort_in_thread<EPT, (EPT > 4 ? 4 : 0)>(a, b, size);
+        else if (stride == 2)
+          sort_in_thread<EPT, (EPT > 2 ? 2 : 0)>(a, b, size);
+        else
+          sort_in_thread<EPT, (EPT > 1 ? 1 : 0)>(a, b, size);
+        continue;
+      }
+      const bool lower_lane = stride < 32u * EPT ? (t & (stride / EPT)) == 0 : false;
+      if (stride >= 32u * EPT) {
+#pragma unroll
+        for (int r = 0; r < EPT; ++r) {
+          s1[t * EPT + r] = a[r];
+          s2[t * EPT + r] = b[r];
+        }
+        __syncthreads();
+      }
+#pragma unroll
+      for (int r = 0; r < EPT; ++r) {
+        const uint32_t e = t * (uint32_t)EPT + (uint32_t)r;
+        uint64_t oa, ob;
+        bool lower;
+        if (stride < 32u * EPT) {
+          oa = __shfl_xor_sync(kFull, a[r], stride / EPT);
+          ob = __shfl_xor_sync(kFull, b[r], stride / EPT);
+          lower = lower_lane;
+        } else {
+          oa = s1[e ^ stride];
+          ob = s2[e ^ stride];
+          lower = (e & stride) == 0;
+        }
+        const bool up = (e & size) == 0;
+        const bool other_less = oa < a[r] || (oa == a[r] && ob < b[r]);
+        if ((lower == up) == other_less) {
+          a[r] = oa;
+          b[r] = ob;
+        }
+      }
+      if (stride >= 32u * EPT)
+        __syncthreads(); // s1 / s2 are rewritten by the next such stage
     }
   }
 }
@@ -831,7 +941,8 @@ __host__ __device__ inline uint32_t next_pow2(uint32_t x)
 __host__ __device__ inline uint32_t sort_scratch_bytes(uint32_t m, int rank_bits)
 {
   const uint32_t n2 = next_pow2(m < 2 ? 2 : m);
-  return rank_bits > 32 ? n2 * 16u : n2 * 12u;
+  (void)rank_bits;
+  return (n2 > kSortLanes ? n2 : kSortLanes) * 16u; // two 64-bit words per element, at least one per thread
 }
 
 // ---------------------------------------------------------------------------
@@ -944,16 +1055,67 @@ __device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, cons
   }
 }
 
-// Sort the m items (raw[i], idx[i]) (i < m) and write them to the output
-// slots of one segment. `scratch` must hold sort_scratch_bytes(m) bytes and
-// the items must be visible to the whole block.
+// Sort the m items (raw[i], idx[i]) (i < m) by (rank, source index), the
+// stable_sorted order of "Top-K: Determinism, Tie-Breaking, and Output
+// Ordering" (Output ordering table), and write them to the output slots of
+// one segment: a register bitonic sort of EPT elements per thread (items
+// padded with keys that sort last); sort_and_write below picks it for up to
+// one item per thread. Ranks up to 32 bits sort as one 64-bit
+// composite rank<<32 | index with the item's slot beside it; 64-bit ranks as
+// (rank, index<<32 | slot). `scratch` holds sort_scratch_bytes(m) bytes; the
+// items must be visible to the whole block.
+template <class TR, int NT, int EPT>
+__device__ __forceinline__ void sort_write_ept(const typename TR::Raw* raw, const uint32_t* idx, uint32_t m,
+                                               typename TR::Rank dirmask, unsigned char* scratch,
+                                               typename TR::Raw* out_keys, int32_t* out_values,
+                                               const int32_t* values)
+{
+  uint64_t a[EPT], b[EPT];
+#pragma unroll
+  for (int r = 0; r < EPT; ++r) {
+    const uint32_t e = threadIdx.x * (uint32_t)EPT + (uint32_t)r;
+    a[r] = ~0ull;
+    b[r] = ~0ull;
+    if (e < m) {
+      const uint64_t rk = (uint64_t)TR::rank(raw[e], dirmask);
+      if constexpr (TR::kRankBits <= 32) {
+        a[r] = (rk << 32) | idx[e];
+        b[r] = e;
+      } else {
+        a[r] = rk;
+        b[r] = ((uint64_t)idx[e] << 32) | e;
+      }
+    }
+  }
+  uint64_t* s1 = reinterpret_cast<uint64_t*>(scratch);
+  uint64_t* s2 = s1 + (uint32_t)EPT * NT;
+  reg_bitonic_sort<NT, EPT>(a, b, s1, s2);
+#pragma unroll
+  for (int r = 0; r < EPT; ++r) {
+    const uint32_t e = threadIdx.x * (uint32_t)EPT + (uint32_t)r;
+    if (e < m) {
+      const uint32_t slot = (uint32_t)b[r];
+      out_keys[e] = raw[slot];
+      if (out_values)
+        out_values[e] = values[idx[slot]];
+    }
+  }
+}
+
 template <class TR, int NT>
 __device__ __forceinline__ void sort_and_write(const typename TR::Raw* raw, const uint32_t* idx, uint32_t m,
-                                            typename TR::Rank dirmask, unsigned char* scratch,
-                                            typename TR::Raw* out_keys, int32_t* out_values,
-                                            const int32_t* values)
+                                               typename TR::Rank dirmask, unsigned char* scratch,
+                                               typename TR::Raw* out_keys, int32_t* out_values,
+                                               const int32_t* values)
 {
+  static_assert(NT == (int)kSortLanes, "sort scratch is sized for kSortLanes threads");
   const uint32_t n2 = next_pow2(m < 2 ? 2 : m);
+  if (n2 <= (uint32_t)NT) {
+    // one item per thread: registers and shuffles (measured faster up to 256
+    // items; above, the shared-memory network below is)
+    sort_write_ept<TR, NT, 1>(raw, idx, m, dirmask, scratch, out_keys, out_values, values);
+    return;
+  }
   if constexpr (TR::kRankBits <= 32) {
     uint64_t* key = reinterpret_cast<uint64_t*>(scratch);
     uint32_t* pay = reinterpret_cast<uint32_t*>(key + n2);
