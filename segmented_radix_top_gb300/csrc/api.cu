@@ -82,10 +82,6 @@ struct Plan {
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Margin of the speculative bound with several waves of segments.
-constexpr float kSpecZ = 2.0f;
-constexpr float kSpecC = 1.0f;
-
 // Largest C * k for which the cluster gathers whole candidate lists.
 constexpr uint32_t kGatherListsMaxItems = 512;
 // Largest C * k for which the cluster gathers local top-k lists into the leader.
@@ -357,8 +353,13 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
   // a slice whose bound proves too tight is read twice, which with one wave
   // sets the kernel's time (wide margin) and with many waves is averaged out
   // (narrower margin, shorter lists).
-  p.spec_z = pl.waves <= 1 ? 4.0f : kSpecZ;
-  p.spec_c = pl.waves <= 1 ? 3.0f : kSpecC;
+  // How: warp minimums (the exact target, cheap) with one wave and for 64-bit
+  // ranks; digit passes that may stop with up to twice the target (suits
+  // keys with many duplicates) for narrower keys over several waves. The
+  // exact target wants the wider margin.
+  p.spec_small = (pl.waves <= 1 || ops.rank_bits == 64) ? 1 : 0;
+  p.spec_z = pl.waves <= 1 ? 4.0f : (p.spec_small ? 3.0f : 2.0f);
+  p.spec_c = pl.waves <= 1 ? 3.0f : (p.spec_small ? 2.0f : 1.0f);
   p.ring_stages = kStages;
   p.ring_bytes = pl.ring_bytes;
   p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;

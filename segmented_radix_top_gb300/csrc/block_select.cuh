@@ -53,6 +53,7 @@ struct Ctrl {
   uint32_t gather_count;             // cluster leader: entries gathered from the cluster
   uint32_t front_base;               // cross-CTA scan: selected entries of preceding CTAs
   uint32_t tie_base;                 // cross-CTA scan: boundary ties of preceding CTAs
+  uint32_t spec_kept;                // small speculative selection: sample keys kept
   uint64_t xb[16][2];                // cluster leader: every CTA's local k-th (rank, preference index)
   uint64_t xb_min[2];                // the cluster-wide minimum of xb
 };
@@ -764,6 +765,116 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t
     return Spec<Rank>{false, (Rank)0, 0u, pass};
   const Kept<Rank> kp = select_into<TR, NT>(ctl, pass, src, s, dst_raw, dst_idx, cap, dirmask, false);
   return Spec<Rank>{true, edge, kp.n, pass};
+}
+
+// The speculative first bound for a small target (mm <= 32) and a sample of
+// ring keys only, without digit passes: every thread sorts its (up to 8)
+// sample keys in registers, every warp extracts its mm smallest by repeated
+// warp minimums, and one warp merges the warps' sorted lists the same way;
+// the mm-th smallest is exact because the sample's mm smallest lie among
+// the warps' mm smallest. Selection keys are 32 bits: the rank, or its high
+// word for 64-bit ranks (resolution enough for a first bound). Every sample
+// key at or below the edge is written to dst, as spec_into does; `stage` is
+// 1 KiB of free shared memory. Fails (nothing usable written) on heavy ties
+// at the edge (more than 2 mm + 64 keys kept) or an edge at the worst rank.
+template <class TR, int NT>
+__device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_t pass, const typename TR::Raw* sample,
+                                                              uint32_t idx0, uint32_t ns, uint32_t mm,
+                                                              typename TR::Raw* dst_raw, uint32_t* dst_idx,
+                                                              uint32_t cap, typename TR::Rank dirmask,
+                                                              uint32_t* stage)
+{
+  using Rank = typename TR::Rank;
+  constexpr int KPT = 8;
+  constexpr int NW = NT / 32;
+  static_assert(NW <= 32, "one merge lane per warp");
+  auto key32 = [&](uint32_t e) -> uint32_t {
+    const Rank r = TR::rank(sample[e], dirmask);
+    if constexpr (TR::kRankBits == 64)
+      return (uint32_t)(r >> 32);
+    else
+      return (uint32_t)r;
+  };
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  uint32_t v[KPT];
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const uint32_t e = (uint32_t)i * NT + threadIdx.x;
+    v[i] = e < ns ? key32(e) : ~0u;
+  }
+  // odd-even transposition sort of the thread's keys
+#pragma unroll
+  for (int round = 0; round < KPT; ++round) {
+#pragma unroll
+    for (int i = round & 1; i + 1 < KPT; i += 2) {
+      const uint32_t lo = min(v[i], v[i + 1]), hi = max(v[i], v[i + 1]);
+      v[i] = lo;
+      v[i + 1] = hi;
+    }
+  }
+  // the warp's mm smallest, in order
+  for (uint32_t it = 0; it < mm; ++it) {
+    const uint32_t mn = __reduce_min_sync(kFull, v[0]);
+    const uint32_t win = __ffs(__ballot_sync(kFull, v[0] == mn)) - 1;
+    if (lane == win) {
+#pragma unroll
+      for (int i = 0; i + 1 < KPT; ++i)
+        v[i] = v[i + 1];
+      v[KPT - 1] = ~0u;
+    }
+    if (lane == 0)
+      stage[warp * 32u + it] = mn;
+  }
+  if (threadIdx.x == 0)
+    ctl.spec_kept = 0;
+  __syncthreads();
+  // warp 0 merges the NW sorted lists: the mm-th smallest overall
+  if (warp == 0) {
+    uint32_t p = 0;
+    uint32_t head = lane < (uint32_t)NW ? stage[lane * 32u] : ~0u;
+    uint32_t edge = ~0u;
+    for (uint32_t it = 0; it < mm; ++it) {
+      const uint32_t mn = __reduce_min_sync(kFull, head);
+      const uint32_t win = __ffs(__ballot_sync(kFull, head == mn)) - 1;
+      edge = mn;
+      if (lane == win) {
+        ++p;
+        head = p < mm ? stage[lane * 32u + p] : ~0u;
+      }
+    }
+    if (lane == 0)
+      ctl.res[0] = edge;
+  }
+  __syncthreads();
+  const uint32_t e32 = ctl.res[0];
+  // every sample key at or below the edge into dst (warp-aggregated slots)
+#pragma unroll
+  for (int i = 0; i < KPT; ++i) {
+    const uint32_t e = (uint32_t)i * NT + threadIdx.x;
+    const bool keep = e < ns && key32(e) <= e32;
+    const uint32_t bal = __ballot_sync(kFull, keep);
+    if (bal) {
+      uint32_t wb = 0;
+      if (lane == 0)
+        wb = atomicAdd(&ctl.spec_kept, __popc(bal));
+      const uint32_t pos = __shfl_sync(kFull, wb, 0) + __popc(bal & lanemask_lt());
+      if (keep && pos < cap) {
+        dst_raw[pos] = sample[e];
+        dst_idx[pos] = idx0 + e;
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t kept = ctl.spec_kept;
+  __syncthreads(); // ctl.res and the stage are free again
+  Rank edge;
+  if constexpr (TR::kRankBits == 64)
+    edge = ((Rank)e32 << 32) | 0xffffffffull;
+  else
+    edge = (Rank)e32;
+  constexpr Rank kWorst = (TR::kRankBits == 64) ? ~(Rank)0 : (Rank)(((uint64_t)1 << TR::kRankBits) - 1);
+  const bool ok = edge < kWorst && kept <= 2u * mm + 64u && kept <= cap;
+  return Spec<Rank>{ok, edge, kept, pass};
 }
 
 // ---------------------------------------------------------------------------

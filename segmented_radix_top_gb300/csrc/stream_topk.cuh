@@ -75,6 +75,7 @@ struct KernelParams {
   uint32_t spec_keys;    // sample size of the speculative first bound
   float spec_z;          // its margin: mu + spec_z * sqrt(mu) + spec_c sample keys are kept
   float spec_c;
+  int32_t spec_small;    // small targets by warp minimums (exact) rather than digit passes (slack stop)
 };
 
 // Host and device agree on the dynamic shared-memory layout.
@@ -456,11 +457,15 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
             const uint32_t mm = (uint32_t)ceilf(mu + p.spec_z * sqrtf(mu) + p.spec_c);
             if (mm < k && mm < ns) {
               const uint32_t b0 = fwd ? 0u : nv - nbs;
+              // a small target over ring keys only: warp minimums; else digit passes
               const Spec<Rank> sp =
-                spec_into<TR, NT>(ctl, sel_pass,
-                                  Src<Raw>{list_raw, list_idx, count, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK,
-                                           nbs * VK},
-                                  spare_raw, spare_idx, mm, L, dirmask, cbuf);
+                (p.spec_small && count == 0 && mm <= 32u && nbs * VK <= 8u * NT)
+                  ? spec_small<TR, NT>(ctl, sel_pass, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nbs * VK, mm,
+                                       spare_raw, spare_idx, L, dirmask, reinterpret_cast<uint32_t*>(cbuf.pos))
+                  : spec_into<TR, NT>(ctl, sel_pass,
+                                      Src<Raw>{list_raw, list_idx, count, stage_keys + (size_t)b0 * VK,
+                                               idx0 + b0 * VK, nbs * VK},
+                                      spare_raw, spare_idx, mm, L, dirmask, cbuf);
               sel_pass = sp.pass;
               if (sp.ok) {
                 swap_lists();
