@@ -710,6 +710,53 @@ __device__ __forceinline__ Kept<typename TR::Rank> trim_into(Ctrl& ctl, uint32_t
   return select_into<TR, NT>(ctl, pass, src, s, dst_raw, dst_idx, kk + slack, dirmask, prefer_larger);
 }
 
+// The kk best of ring keys only (src.count == 0) when their kk-th key is
+// expected to lie in a block of keys tied at rank e (a speculative
+// selection just met that block): one count of the keys better than e and
+// equal to it, and if the kk-th key is indeed a tie, the better keys and the
+// first kk - better ties in preference order (select_ties_ordered) written
+// to dst -- no digit passes. Returns n == 0 if the kk-th key is not a tie.
+template <class TR, int NT>
+__device__ __forceinline__ Kept<typename TR::Rank> tie_block_into(Ctrl& ctl, uint32_t pass,
+                                                                  const Src<typename TR::Raw>& src,
+                                                                  typename TR::Rank e, uint32_t kk,
+                                                                  typename TR::Raw* dst_raw, uint32_t* dst_idx,
+                                                                  uint32_t cap, typename TR::Rank dirmask,
+                                                                  bool prefer_larger)
+{
+  using Rank = typename TR::Rank;
+  if (threadIdx.x == 0) {
+    // select_into counts in the slot of the last digit pass; none ran here
+    PassSlot& sl = ctl.slot[(pass + 2) % 3];
+    sl.kept = 0;
+    sl.kmax = 0;
+  }
+  const uint32_t n = src.ext_count;
+  uint32_t f = 0, t = 0;
+  for (uint32_t i = threadIdx.x; i < n; i += NT) {
+    const Rank r = TR::rank(src.ext_raw[i], dirmask);
+    f += r < e ? 1u : 0u;
+    t += r == e ? 1u : 0u;
+  }
+  f = __reduce_add_sync(kFull, f);
+  t = __reduce_add_sync(kFull, t);
+  if (lane_id() == 0)
+    ctl.red[threadIdx.x >> 5] = ((uint64_t)f << 32) | t;
+  __syncthreads();
+  uint32_t front = 0, ties = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    front += (uint32_t)(ctl.red[w] >> 32);
+    ties += (uint32_t)ctl.red[w];
+  }
+  __syncthreads(); // ctl.red is free again
+  if (!(front < kk && kk <= front + ties && kk <= cap))
+    return Kept<Rank>{(Rank)0, 0u, pass};
+  Selection<Rank> s{e, ~(Rank)0, 0u, 0u, kk};
+  select_ties_ordered<TR, NT>(ctl, src, kk - front, dirmask, prefer_larger, s);
+  return select_into<TR, NT>(ctl, pass, src, s, dst_raw, dst_idx, cap, dirmask, prefer_larger);
+}
+
 // A speculative first bound from a sample of a slice: the smallest rank
 // edge with at least mm sample entries at or below it (mm is below the
 // number the slice needs), found by a digit selection that may stop early
@@ -726,6 +773,7 @@ struct Spec {
   Rank edge;
   uint32_t n;
   uint32_t pass;
+  bool tie_block; // failed on a block of keys tied at rank `edge` (an exact rank)
 };
 template <class TR, int NT>
 __device__ __forceinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t pass, const Src<typename TR::Raw> src,
@@ -762,9 +810,9 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t
     s = Selection<Rank>{rr.prefix, rr.mask, 0u, 0u, total}; // the whole boundary bucket
   }
   if (!ok || edge == kWorst || total > cap)
-    return Spec<Rank>{false, (Rank)0, 0u, pass};
+    return Spec<Rank>{false, (Rank)0, 0u, pass, false};
   const Kept<Rank> kp = select_into<TR, NT>(ctl, pass, src, s, dst_raw, dst_idx, cap, dirmask, false);
-  return Spec<Rank>{true, edge, kp.n, pass};
+  return Spec<Rank>{true, edge, kp.n, pass, false};
 }
 
 // The speculative first bound for a small target (mm <= 32) and a sample of
@@ -776,7 +824,8 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t
 // word for 64-bit ranks (resolution enough for a first bound). Every sample
 // key at or below the edge is written to dst, as spec_into does; `stage` is
 // 1 KiB of free shared memory. Fails (nothing usable written) on heavy ties
-// at the edge (more than 2 mm + 64 keys kept) or an edge at the worst rank.
+// at the edge (the target's value also at half the target, or more than
+// 2 mm + 64 keys kept) or an edge at the worst rank.
 template <class TR, int NT>
 __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_t pass, const typename TR::Raw* sample,
                                                               uint32_t idx0, uint32_t ns, uint32_t mm,
@@ -832,21 +881,29 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_
   if (warp == 0) {
     uint32_t p = 0;
     uint32_t head = lane < (uint32_t)NW ? stage[lane * 32u] : ~0u;
-    uint32_t edge = ~0u;
+    uint32_t edge = ~0u, mid = ~0u;
     for (uint32_t it = 0; it < mm; ++it) {
       const uint32_t mn = __reduce_min_sync(kFull, head);
       const uint32_t win = __ffs(__ballot_sync(kFull, head == mn)) - 1;
       edge = mn;
+      if (it == (mm - 1) / 2)
+        mid = mn;
       if (lane == win) {
         ++p;
         head = p < mm ? stage[lane * 32u + p] : ~0u;
       }
     }
-    if (lane == 0)
+    if (lane == 0) {
       ctl.res[0] = edge;
+      ctl.res[1] = (mm > 2u && mid == edge) ? 1u : 0u; // the target's value fills half of it: a tie block
+    }
   }
   __syncthreads();
   const uint32_t e32 = ctl.res[0];
+  if (ctl.res[1]) {
+    __syncthreads(); // ctl.res and the stage are free again
+    return Spec<Rank>{false, (Rank)e32, 0u, pass, TR::kRankBits <= 32};
+  }
   // every sample key at or below the edge into dst (warp-aggregated slots)
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {
@@ -873,8 +930,9 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_
   else
     edge = (Rank)e32;
   constexpr Rank kWorst = (TR::kRankBits == 64) ? ~(Rank)0 : (Rank)(((uint64_t)1 << TR::kRankBits) - 1);
-  const bool ok = edge < kWorst && kept <= 2u * mm + 64u && kept <= cap;
-  return Spec<Rank>{ok, edge, kept, pass};
+  const bool ties = kept > 2u * mm + 64u || kept > cap;
+  const bool ok = edge < kWorst && !ties;
+  return Spec<Rank>{ok, edge, kept, pass, ties && TR::kRankBits <= 32};
 }
 
 // ---------------------------------------------------------------------------

@@ -450,6 +450,8 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
           // the exact k best of enough to pass k, at least kBootKeys
           uint32_t nb = 0;
           bool done = false;
+          bool tie_block = false; // the speculative selection met a tie block at rank tie_rank
+          Rank tie_rank = 0;
           if (allow_spec) {
             const uint32_t nbs = min(nv, (p.spec_keys + VK - 1) / VK);
             const uint32_t ns = count + nbs * VK;
@@ -467,6 +469,8 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
                                                idx0 + b0 * VK, nbs * VK},
                                       spare_raw, spare_idx, mm, L, dirmask, cbuf);
               sel_pass = sp.pass;
+              tie_block = sp.tie_block;
+              tie_rank = sp.edge;
               if (sp.ok) {
                 swap_lists();
                 set_bound(sp.edge + 1, sp.n); // accept rank <= edge
@@ -483,7 +487,22 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
             const uint32_t want = max(k + 1 - count, max(4u * k, (uint32_t)kBootKeys));
             nb = min(nv, (want + VK - 1) / VK);
             const uint32_t b0 = fwd ? 0u : nv - nb;
-            select_union(stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nb * VK, trim_slack);
+            bool tied = false;
+            if (tie_block && count == 0) {
+              // the k-th key probably lies in the tie block just met: the keys
+              // better than it and the first ties in preference order
+              const Kept<Rank> kp =
+                tie_block_into<TR, NT>(ctl, sel_pass, Src<Raw>{list_raw, list_idx, 0u, stage_keys + (size_t)b0 * VK,
+                                                                idx0 + b0 * VK, nb * VK},
+                                       tie_rank, k, spare_raw, spare_idx, L, dirmask, pl);
+              if (kp.n) {
+                swap_lists();
+                set_bound(kp.max_rank, kp.n);
+                tied = true;
+              }
+            }
+            if (!tied)
+              select_union(stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nb * VK, trim_slack);
           }
           if (nb < nv)
             process_vectors(stage, fwd ? nb : 0u, fwd ? nv : nv - nb, idx0);
