@@ -175,6 +175,51 @@ int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* keys, const i
                               void* out_keys, int32_t* out_values, int64_t max_segment_len,
                               void* device_workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Size of the fixed device staging area of segtopk_batched_topk_host_noalloc:
+ * 32 MiB. A request fits when segtopk_host_workspace_bytes(...) for its
+ * sizes is at most this (for example about 4 million fp32 keys with int32
+ * values, or 8 million fp32 keys alone).
+ */
+#define SEGTOPK_NOALLOC_STAGING_BYTES (32u * 1024u * 1024u)
+
+/*
+ * segtopk_batched_topk_host for callers that cannot allocate device memory:
+ * a plugin or library routine running inside a host program that owns the
+ * GPU's memory (a framework whose caching allocator has reserved it, so that
+ * a cudaMalloc of the caller's own would fail or fragment that pool), or
+ * code held to a fixed device-memory budget with no per-call allocations.
+ * The source pages have no counterpart of this entry point.
+ *
+ * Arguments, semantics and results are those of segtopk_batched_topk_host,
+ * without the workspace: the device staging comes from a fixed array of
+ * SEGTOPK_NOALLOC_STAGING_BYTES inside the library. Every GPU on which the
+ * library's device code is loaded holds that array until the process exits.
+ * The call runs on the current device, which must be the device of `stream`.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address once; make that first call before any stream
+ * capture begins on the device.
+ *
+ * Limits and errors: a request needing more than SEGTOPK_NOALLOC_STAGING_BYTES
+ * of staging returns SEGTOPK_ERROR_NOT_SUPPORTED before anything is copied.
+ * Otherwise the status codes are those of segtopk_batched_topk_host. The call
+ * makes no device allocation and frees nothing.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's data; each call writes every byte it reads from it, so nothing needs
+ * clearing. Calls whose GPU work overlaps (calls from several host threads,
+ * or on several streams of one device) race on the array: serialise them.
+ * Like segtopk_batched_topk_host, the call waits for `stream` before it
+ * returns.
+ */
+int segtopk_batched_topk_host_noalloc(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+                                      const int64_t* segment_offsets, int64_t num_segments, int32_t k,
+                                      segtopk_direction direction, segtopk_determinism determinism,
+                                      segtopk_tie_break tie_break, segtopk_ordering ordering,
+                                      void* out_keys, int32_t* out_values, int64_t max_segment_len,
+                                      void* stream);
+
 /* Device workspace bytes segtopk_batched_topk_host needs for these sizes
  * (num_keys = number of key elements the offsets address, i.e. the largest
  * segment end). Host-only arithmetic. */

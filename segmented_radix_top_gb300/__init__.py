@@ -5,8 +5,9 @@ include/segtopk.h (libsegtopk.so); this package only marshals tensors into
 that ABI (see _binding.py) and provides the seeded synthetic workloads
 (workloads.py).
 """
-from ._binding import (DETERMINISM, DIRECTION, DTYPE, KEY_BYTES, MAX_K, ORDERING, TIE_BREAK,  # noqa: F401
-                       SegTopKError, batched_topk, batched_topk_host, host_workspace_bytes,
+from ._binding import (DETERMINISM, DIRECTION, DTYPE, KEY_BYTES, MAX_K, NOALLOC_STAGING_BYTES,  # noqa: F401
+                       ORDERING, TIE_BREAK, SegTopKError, batched_topk, batched_topk_host,
+                       batched_topk_host_noalloc, host_workspace_bytes,
                        last_launch_count, library_path, load, read_device_error)
 
 

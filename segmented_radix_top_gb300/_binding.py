@@ -23,6 +23,7 @@ ORDERING = {"unsorted": 0, "sorted": 1, "stable_sorted": 2}
 STATUS = {0: "SUCCESS", 1: "INVALID_VALUE", 2: "INVALID_COMBINATION", 3: "NOT_SUPPORTED",
           4: "MISALIGNED", 5: "CUDA", 6: "DEVICE"}
 MAX_K = 2048
+NOALLOC_STAGING_BYTES = 32 * 1024 * 1024  # SEGTOPK_NOALLOC_STAGING_BYTES
 
 _TORCH_TO_DTYPE = {torch.float16: "f16", torch.bfloat16: "bf16", torch.float32: "f32",
                    torch.float64: "f64", torch.int32: "i32"}
@@ -68,6 +69,9 @@ def load():
     L.segtopk_batched_topk_host.restype = c_int
     L.segtopk_batched_topk_host.argtypes = [c_int, vp, vp, vp, c_i64, c_i32, c_int, c_int, c_int,
                                             c_int, vp, vp, c_i64, vp, ctypes.c_size_t, vp]
+    L.segtopk_batched_topk_host_noalloc.restype = c_int
+    L.segtopk_batched_topk_host_noalloc.argtypes = [c_int, vp, vp, vp, c_i64, c_i32, c_int, c_int, c_int,
+                                                    c_int, vp, vp, c_i64, vp]
     L.segtopk_host_workspace_bytes.restype = ctypes.c_size_t
     L.segtopk_host_workspace_bytes.argtypes = [c_int, c_int, c_i64, c_i64, c_i32]
     L.segtopk_status_string.restype = ctypes.c_char_p
@@ -173,6 +177,32 @@ def batched_topk_host(key_dtype: str, keys: torch.Tensor, segment_offsets: torch
                                      ORDERING[ordering], _ptr(out_keys), _ptr(out_values), ml,
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream_handle(stream, workspace.device))
+    _check(rc)
+    return out_keys, out_values
+
+
+def batched_topk_host_noalloc(key_dtype: str, keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *,
+                              values=None, direction: str = "max", determinism: str = "gpu_to_gpu",
+                              tie_break: str = "prefer_smaller_index", ordering: str = "stable_sorted",
+                              out_keys=None, out_values=None, max_segment_len: int | None = None,
+                              stream=None, device=None):
+    """Host-buffer variant that allocates no device memory: the library stages
+    the call in its own fixed device array of NOALLOC_STAGING_BYTES (for
+    callers that cannot allocate). Runs on the current CUDA device (or
+    `device`); synchronises before returning; calls must not overlap."""
+    L = load()
+    num_segments = segment_offsets.numel() - 1
+    if out_keys is None:
+        out_keys = torch.empty(num_segments * k, dtype=keys.dtype)
+    if values is not None and out_values is None:
+        out_values = torch.empty(num_segments * k, dtype=torch.int32)
+    ml = -1 if max_segment_len is None else int(max_segment_len)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    rc = L.segtopk_batched_topk_host_noalloc(DTYPE[key_dtype], _ptr(keys), _ptr(values), _ptr(segment_offsets),
+                                             num_segments, int(k), DIRECTION[direction],
+                                             DETERMINISM[determinism], TIE_BREAK[tie_break],
+                                             ORDERING[ordering], _ptr(out_keys), _ptr(out_values), ml,
+                                             _stream_handle(stream, dev))
     _check(rc)
     return out_keys, out_values
 

@@ -267,6 +267,11 @@ int validate(int dtype, const void* keys, const int32_t* values, const int64_t* 
 }
 
 } // namespace
+
+// Records a failed CUDA call for segtopk_last_cuda_error on this thread (for
+// the library's other translation units); returns SEGTOPK_ERROR_CUDA.
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 } // namespace segtopk
 
 using namespace segtopk;

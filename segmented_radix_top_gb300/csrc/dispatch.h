@@ -37,4 +37,7 @@ const KeyOps& key_ops_f64();
 const KeyOps& key_ops_u32();
 const KeyOps& key_ops_i32();
 
+// Records a failed CUDA call for segtopk_last_cuda_error; returns SEGTOPK_ERROR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 } // namespace segtopk
