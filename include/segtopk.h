@@ -145,13 +145,33 @@ typedef struct {
    * (fewest waves, ties toward the widest cluster); 1..16 forces the width
    * (widths above 8 need non-portable cluster support). */
   int32_t cluster_width;
-  int32_t reserved[7]; /* must be zero */
+  /* Warp-select paths (used when k <= 32): segments of at most
+   * small_segment_max_len keys take one warp each, longer ones of at most
+   * team_segment_max_len keys a team of eight warps each; longer segments
+   * (and every segment when k > 32) take one CTA or cluster each. 0 chooses
+   * the defaults below (none when cluster_width is forced); a negative value
+   * turns that path off. */
+  int32_t small_segment_max_len;
+  int32_t team_segment_max_len;
+  int32_t reserved[5]; /* must be zero */
 } segtopk_options;
+
+/* Default limits of the warp-select paths. With at least as many segments as
+ * SMs: one warp per segment up to SEGTOPK_SMALL_SEGMENT_DEFAULT keys and no
+ * team range (SEGTOPK_TEAM_SEGMENT_DEFAULT does not exceed it: longer
+ * segments are faster on the CTA path then). With fewer segments: no
+ * single-warp range and teams of eight warps up to SEGTOPK_TEAM_SEGMENT_FEW
+ * keys. */
+#define SEGTOPK_SMALL_SEGMENT_DEFAULT 4096
+#define SEGTOPK_TEAM_SEGMENT_DEFAULT 4096
+#define SEGTOPK_TEAM_SEGMENT_FEW 8192
 
 /* segtopk_batched_topk with launch controls; options may be NULL. Returns
  * SEGTOPK_ERROR_INVALID_VALUE for a width outside 0..16 or nonzero reserved
  * fields, and SEGTOPK_ERROR_NOT_SUPPORTED when the device cannot launch the
- * requested width. */
+ * requested width. Without options (and in segtopk_batched_topk), the
+ * warp-select paths take the segments their default limits give when
+ * k <= 32; the others take one CTA or cluster each. */
 int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
                             const int64_t* segment_offsets, int64_t num_segments, int32_t k,
                             segtopk_direction direction, segtopk_determinism determinism,

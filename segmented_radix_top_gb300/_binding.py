@@ -39,7 +39,8 @@ class SegTopKError(RuntimeError):
 
 
 class Options(ctypes.Structure):
-    _fields_ = [("cluster_width", ctypes.c_int32), ("reserved", ctypes.c_int32 * 7)]
+    _fields_ = [("cluster_width", ctypes.c_int32), ("small_segment_max_len", ctypes.c_int32),
+                ("team_segment_max_len", ctypes.c_int32), ("reserved", ctypes.c_int32 * 5)]
 
 
 _lib = None
@@ -119,7 +120,8 @@ def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, v
                  direction: str = "max", determinism: str = "gpu_to_gpu",
                  tie_break: str = "prefer_smaller_index", ordering: str = "stable_sorted",
                  out_keys=None, out_values=None, max_segment_len: int | None = None,
-                 key_dtype: str | None = None, stream=None, cluster_width: int = 0):
+                 key_dtype: str | None = None, stream=None, cluster_width: int = 0,
+                 small_segment_max_len: int = 0, team_segment_max_len: int = 0):
     """Segmented top-k on the GPU through libsegtopk (see include/segtopk.h).
 
     keys: 1-D CUDA tensor (16-byte aligned); its element size must match the
@@ -128,6 +130,10 @@ def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, v
     Returns (out_keys, out_values) of shape [num_segments * k]; out_values is
     None for keys-only calls. Slots past a short segment's length are left as
     they were in the given out tensors (uninitialised if allocated here).
+    cluster_width forces the CTAs per segment (0: automatic);
+    small_segment_max_len / team_segment_max_len set which segments take one
+    warp / a team of eight warps each when k <= 32 (0: the defaults, or none
+    with a forced width; < 0: none).
     """
     L = load()
     kd = key_dtype_of(keys, key_dtype)
@@ -141,6 +147,8 @@ def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, v
     ml = -1 if max_segment_len is None else int(max_segment_len)
     opts = Options()
     opts.cluster_width = int(cluster_width)
+    opts.small_segment_max_len = int(small_segment_max_len)
+    opts.team_segment_max_len = int(team_segment_max_len)
     rc = L.segtopk_batched_topk_ex(DTYPE[kd], _ptr(keys), _ptr(values), _ptr(segment_offsets),
                                    num_segments, int(k), DIRECTION[direction],
                                    DETERMINISM[determinism], TIE_BREAK[tie_break], ORDERING[ordering],

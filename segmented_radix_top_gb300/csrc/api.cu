@@ -11,6 +11,7 @@
 #include "block_select.cuh"
 #include "dispatch.h"
 #include "stream_topk.cuh"
+#include "warp_topk.cuh"
 
 namespace segtopk {
 namespace {
@@ -285,6 +286,7 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
 {
   t_last_launch_count = 0;
   int forced_width = 0;
+  int32_t small_max = 0, team_max = 0;
   if (options) {
     for (int r : options->reserved)
       if (r != 0)
@@ -292,6 +294,8 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
     if (options->cluster_width < 0 || options->cluster_width > 16)
       return SEGTOPK_ERROR_INVALID_VALUE;
     forced_width = options->cluster_width;
+    small_max = options->small_segment_max_len;
+    team_max = options->team_segment_max_len;
   }
   int v = validate(key_dtype, keys, values, segment_offsets, num_segments, k, direction, determinism,
                    tie_break, ordering, out_keys, out_values, max_segment_len);
@@ -304,6 +308,19 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
   if (dev.major != 10 || dev.minor != 3)
     return SEGTOPK_ERROR_DEVICE;
   cudaStream_t st = (cudaStream_t)stream;
+  // Warp-select limits (k <= 32). With many segments, single warps for short
+  // ones and the CTA path above (measured faster than teams there); with
+  // fewer segments than SMs the latency of one segment sets the time, so
+  // short segments take teams of eight warps and long ones the CTA path.
+  const bool few = num_segments < (int64_t)dev.sms;
+  if (small_max == 0)
+    small_max = (forced_width > 0 || few) ? -1 : SEGTOPK_SMALL_SEGMENT_DEFAULT;
+  if (team_max == 0)
+    team_max = forced_width > 0 ? -1 : (few ? SEGTOPK_TEAM_SEGMENT_FEW : SEGTOPK_TEAM_SEGMENT_DEFAULT);
+  if (k > kWarpPathMaxK)
+    small_max = team_max = -1;
+  const int64_t lim1 = small_max > 0 ? small_max : 0;                  // one warp: (0, lim1]
+  const int64_t lim2 = team_max > 0 ? std::max<int64_t>(team_max, lim1) : lim1; // eight warps: (lim1, lim2]
 
   int64_t max_len = max_segment_len;
   if (max_len < 0) {
@@ -324,13 +341,50 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
     return SEGTOPK_SUCCESS;
 
   const KeyOps& ops = *ops_for(key_dtype);
+  const uint64_t dirmask = (direction == SEGTOPK_MAX) ? ~0ull : 0ull;
+  const uint64_t rank_mask = ops.rank_bits == 64 ? ~0ull : ((1ull << ops.rank_bits) - 1);
+  // the CTA / cluster plan for segments beyond the warp-select limits, before
+  // anything is launched (an unservable request launches nothing)
+  const bool need_cta = max_len > lim2;
   Plan pl;
-  bool unsupported = false;
-  e = get_plan(key_dtype, ops, num_segments, max_len, k, forced_width, &pl, &unsupported);
-  if (e != cudaSuccess)
-    return cuda_fail(e);
-  if (unsupported)
-    return SEGTOPK_ERROR_NOT_SUPPORTED;
+  if (need_cta) {
+    bool unsupported = false;
+    e = get_plan(key_dtype, ops, num_segments, max_len, k, forced_width, &pl, &unsupported);
+    if (e != cudaSuccess)
+      return cuda_fail(e);
+    if (unsupported)
+      return SEGTOPK_ERROR_NOT_SUPPORTED;
+  }
+  int launches = 0;
+  for (int team = 0; team < 2; ++team) {
+    // warp-select: segments in (lo, hi], one warp or eight warps each
+    const int64_t lo = team ? lim1 : 0, hi = team ? lim2 : lim1;
+    if (hi <= lo || max_len <= lo)
+      continue;
+    KernelParams w;
+    std::memset(&w, 0, sizeof(w));
+    w.keys = keys;
+    w.values = values;
+    w.offsets = segment_offsets;
+    w.out_keys = out_keys;
+    w.out_values = out_values;
+    w.num_segments = num_segments;
+    w.n_lo = lo;
+    w.n_hi = std::min<int64_t>(hi, max_len);
+    w.dirmask = dirmask & rank_mask;
+    w.k = k;
+    w.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;
+    w.sorted = (ordering != SEGTOPK_UNSORTED) ? 1 : 0;
+    w.flag_overlong = max_len <= hi ? 1 : 0; // longer segments belong to a later launch
+    e = ops.launch_warp[team](w, st);
+    if (e != cudaSuccess)
+      return cuda_fail(e);
+    ++launches;
+  }
+  if (!need_cta) {
+    t_last_launch_count = launches;
+    return SEGTOPK_SUCCESS;
+  }
 
   KernelParams p;
   std::memset(&p, 0, sizeof(p));
@@ -340,13 +394,9 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
   p.out_keys = out_keys;
   p.out_values = out_values;
   p.num_segments = num_segments;
-  p.n_lo = 0;
+  p.n_lo = lim2; // shorter segments took a warp-select path
   p.n_hi = max_len;
-  p.dirmask = (direction == SEGTOPK_MAX) ? ~0ull : 0ull;
-  if (ops.rank_bits == 16)
-    p.dirmask &= 0xffffull;
-  else if (ops.rank_bits == 32)
-    p.dirmask &= 0xffffffffull;
+  p.dirmask = dirmask & rank_mask;
   p.k = k;
   p.list_cap = pl.list_cap;
   p.merge_gather = pl.merge_gather;
@@ -373,7 +423,7 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
   e = ops.launch[pl.shape.profile](p, pl.shape, st);
   if (e != cudaSuccess)
     return cuda_fail(e);
-  t_last_launch_count = 1;
+  t_last_launch_count = launches + 1;
   return SEGTOPK_SUCCESS;
 }
 

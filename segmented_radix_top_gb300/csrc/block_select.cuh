@@ -228,15 +228,23 @@ __device__ __forceinline__ void finish_by_count(Key* stage, uint32_t* nfin, cons
   const Key a = lane < n ? stage[lane] : (Key)0;
   const Key c = lane + 32 < n ? stage[lane + 32] : (Key)0;
   uint32_t la = 0, ea = 0, lc = 0, ec = 0;
-#pragma unroll 8
-  for (uint32_t j = 0; j < 32; ++j) {
+  // staged keys j < n only (often a handful): the first 32 by one shuffle
+  // each, keys 32..63 by a second one only when there are that many
+  const uint32_t n0 = n < 32 ? n : 32u;
+#pragma unroll 4
+  for (uint32_t j = 0; j < n0; ++j) {
     const Key w0 = __shfl_sync(kFull, a, j);
-    const Key w1 = __shfl_sync(kFull, c, j);
-    const bool in0 = j < n, in1 = j + 32 < n;
-    la += (in0 & (w0 < a)) + (in1 & (w1 < a));
-    ea += (in0 & (w0 == a)) + (in1 & (w1 == a));
-    lc += (in0 & (w0 < c)) + (in1 & (w1 < c));
-    ec += (in0 & (w0 == c)) + (in1 & (w1 == c));
+    la += w0 < a;
+    ea += w0 == a;
+    lc += w0 < c;
+    ec += w0 == c;
+  }
+  for (uint32_t j = 32; j < n; ++j) {
+    const Key w1 = __shfl_sync(kFull, c, j - 32);
+    la += w1 < a;
+    ea += w1 == a;
+    lc += w1 < c;
+    ec += w1 == c;
   }
   const bool fa = lane < n && la < krem && krem <= la + ea;
   const bool fc = lane + 32 < n && lc < krem && krem <= lc + ec;

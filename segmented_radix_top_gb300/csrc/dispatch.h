@@ -24,6 +24,10 @@ struct KeyOps {
   int rank_bits;
   // Launch the segment kernel (profile s.profile) over all num_segments segments.
   cudaError_t (*launch[kProfiles])(const KernelParams& p, const LaunchShape& s, cudaStream_t stream);
+  // Launch the warp-select kernel (k <= 32) over all num_segments segments,
+  // one warp per segment ([0]) or a team of eight warps per segment ([1]); it
+  // serves those with p.n_lo < n <= p.n_hi.
+  cudaError_t (*launch_warp[2])(const KernelParams& p, cudaStream_t stream);
   // Resident clusters (cluster > 1) or resident CTAs (cluster == 1) per GPU.
   cudaError_t (*occupancy[kProfiles])(const LaunchShape& s, int* resident);
   // Read and clear this translation unit's device error word (synchronous).

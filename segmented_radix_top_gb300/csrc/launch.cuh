@@ -3,6 +3,7 @@
 
 #include "dispatch.h"
 #include "stream_topk.cuh"
+#include "warp_topk.cuh"
 
 namespace segtopk {
 
@@ -83,6 +84,30 @@ struct StreamLauncher {
   }
 };
 
+template <KeyKind KK, int W>
+struct WarpLauncher {
+  static cudaError_t launch(const KernelParams& p, cudaStream_t stream)
+  {
+    // Static shared memory only: ask for the largest shared-memory carveout,
+    // so that the occupancy the launch bounds allow (32 one-warp CTAs, or four
+    // eight-warp CTAs, per SM) is not cut by a small default carveout.
+    static bool prepared = false;
+    if (!prepared) {
+      cudaError_t e = cudaFuncSetAttribute(warp_topk_kernel<KK, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                           (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess)
+        return e;
+      prepared = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.num_segments, 1, 1); // one segment per CTA
+    cfg.blockDim = dim3(32 * W, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, warp_topk_kernel<KK, W>, p);
+  }
+};
+
 inline cudaError_t read_and_clear(uint32_t* word)
 {
   uint32_t zero = 0;
@@ -102,6 +127,7 @@ inline cudaError_t read_and_clear(uint32_t* word)
                                KeyTraits<KIND>::kRankBits,                                         \
                                {&StreamLauncher<KIND, kCtaThreads, ProfileLong>::launch,           \
                                 &StreamLauncher<KIND, kCtaThreads, ProfileMany>::launch},          \
+                               {&WarpLauncher<KIND, 1>::launch, &WarpLauncher<KIND, kWarpTeam>::launch}, \
                                {&StreamLauncher<KIND, kCtaThreads, ProfileLong>::occupancy,        \
                                 &StreamLauncher<KIND, kCtaThreads, ProfileMany>::occupancy},       \
                                &read_and_clear};                                                   \

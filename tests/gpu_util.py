@@ -26,7 +26,8 @@ def to_device_keys(wl: W.Workload, device="cuda") -> torch.Tensor:
 
 
 def run_gpu(wl: W.Workload, cluster_width: int = 0, max_segment_len="auto", device="cuda",
-            values: np.ndarray | None = "workload", keys_t=None, stream=None):
+            values: np.ndarray | None = "workload", keys_t=None, stream=None, small_segment_max_len: int = 0,
+            team_segment_max_len: int = 0):
     """Returns (out_key_bits [S*k] storage dtype, out_values or None) as numpy."""
     if keys_t is None:
         keys_t = to_device_keys(wl, device)
@@ -44,7 +45,8 @@ def run_gpu(wl: W.Workload, cluster_width: int = 0, max_segment_len="auto", devi
     st.batched_topk(keys_t, offs, k, values=vals_t, key_dtype=wl.dtype, direction=wl.direction,
                     determinism=wl.determinism, tie_break=wl.tie_break, ordering=wl.ordering,
                     out_keys=out_k, out_values=out_v, max_segment_len=ml,
-                    cluster_width=cluster_width, stream=stream)
+                    cluster_width=cluster_width, stream=stream, small_segment_max_len=small_segment_max_len,
+                    team_segment_max_len=team_segment_max_len)
     torch.cuda.synchronize()
     gk = out_k.cpu().numpy().view(W.STORAGE[wl.dtype] if wl.dtype != "i32" else np.uint32)
     if wl.dtype == "i32":
