@@ -95,3 +95,40 @@ def test_workspace_bytes(lib):
     b = st.host_workspace_bytes("f32", True, 1000, 10, 8)
     assert a >= 4000 + 88 + 320 and b >= a + 4000 + 320
     assert st.host_workspace_bytes("f32", True, -1, 10, 8) == 0
+
+
+def _header_text():
+    return re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+
+
+def _header_define(name):
+    m = re.search(r"#define\s+%s\s+\(?([0-9u\s*]+)\)?" % name, _header_text())
+    assert m, name
+    return eval(m.group(1).replace("u", ""))  # plain integer products only
+
+
+def test_options_struct_matches_header():
+    body = re.search(r"typedef struct \{(.*?)\} segtopk_options;", _header_text(), flags=re.S).group(1)
+    fields = re.findall(r"int32_t\s+(\w+)(?:\[(\d+)\])?;", body)
+    want = [(name, ctypes.c_int32 * int(n) if n else ctypes.c_int32) for name, n in fields]
+    got = B.Options._fields_
+    assert [n for n, _ in got] == [n for n, _ in want]
+    assert ctypes.sizeof(B.Options) == sum(ctypes.sizeof(t) for _, t in want) == 32
+
+
+def test_duplicated_constants_match_header():
+    import bench
+    assert B.MAX_K == _header_define("SEGTOPK_MAX_K")
+    assert B.NOALLOC_STAGING_BYTES == _header_define("SEGTOPK_NOALLOC_STAGING_BYTES")
+    assert bench.SMALL_SEGMENT_DEFAULT == _header_define("SEGTOPK_SMALL_SEGMENT_DEFAULT")
+    assert bench.TEAM_SEGMENT_FEW == _header_define("SEGTOPK_TEAM_SEGMENT_FEW")
+
+
+def test_options_reject_nonzero_reserved_fields(lib):
+    vp = ctypes.c_void_p
+    for i in range(len(B.Options().reserved)):
+        o = B.Options()
+        o.reserved[i] = 7
+        rc = lib.segtopk_batched_topk_ex(2, vp(16), None, vp(64), 1, 4, 0, 2, 1, 2, vp(128), None, 100,
+                                         ctypes.byref(o), None)
+        assert rc == 1
