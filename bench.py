@@ -105,11 +105,17 @@ def measured_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources with comments and whitespace removed, so that
+    a profile taken with them stays valid across comment-only edits."""
+    import re
     h = hashlib.sha1()
     for p in sorted(glob.glob(os.path.join(ROOT, "segmented_radix_top_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
-            h.update(f.read())
+        with open(p, encoding="utf-8", errors="replace") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(os.path.basename(p).encode())
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,8 +1,9 @@
-// Small segments: one warp per segment.
+// Short segments with k <= 32: one warp, or a team of eight warps, per segment.
 //
 // A short segment does not need a CTA's streaming ring, digit passes and
 // block barriers: one warp reads it straight from global memory and keeps its
-// k best keys (k <= 32) in registers, one entry per lane, sorted. This is the
+// k best keys (k <= 32) in registers, one entry per lane, sorted (a team
+// splits the segment between its warps and merges their lists). This is the
 // small-segment path of "Implement Segmented TopK using Thread-Block-Clusters"
 // (section 3.4 "Single-CTA path" and the launch classification of section
 // 3.3: segments too small for a cluster are served by a smaller unit).
