@@ -81,7 +81,7 @@ typedef enum {
   SEGTOPK_ERROR_DEVICE = 6               /* current device is not an sm_103 GPU */
 } segtopk_status;
 
-/* Largest k this build serves (the selected items of one segment are held
+/* Largest k this library serves (the selected items of one segment are held
  * and sorted on chip). Calls with a larger k return SEGTOPK_ERROR_NOT_SUPPORTED. */
 #define SEGTOPK_MAX_K 2048
 
