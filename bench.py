@@ -4,14 +4,18 @@
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload 1..5|5det]
 
-A step is one segmented top-k call over the whole batch of the workload
-(default: workload 2, 128 segments x 152,064 fp32 keys ~ N(0,1), k = 50, max,
-pairs with value = source index, gpu_to_gpu + prefer_smaller_index +
-stable_sorted). `value` is keys/s over all ranks with the inputs already in
-HBM; inputs rotate over enough copies that every step reads from HBM, not L2.
-The timed steps are replayed from CUDA graphs of library calls, so host
-launch overhead is not measured. `e2e` is the same metric through the
-host-buffer entry point, host<->device copies included.
+A step is one segmented top-k call over the whole batch of a workload. With
+no --workload every workload is timed in turn (1, 2, 3, 4, 5 and 5det) and
+`per_config` holds each one's line; the headline `value` is workload 5 in
+its deterministic mode (4096 segments x 32,768 f64 keys, k = 256, max,
+gpu_to_gpu + stable_sorted), the largest configuration. `value` is keys/s
+over all ranks with the inputs already in HBM; inputs rotate over enough
+copies that every step reads from HBM, not L2. The timed steps are replayed
+from CUDA graphs of library calls, so host launch overhead is not measured.
+`e2e` is the same metric through the host-buffer entry point,
+host<->device copies included.
+
+--stats prints the per-CTA counters of the instrumented build instead.
 
 --impl reference times the CPU oracle (the only reference this subject has)
 on this machine's host cores, on bounded samples of the same workload.
@@ -257,7 +261,7 @@ def run_reference(args, ws, rank):
         return 0
     import oracle
     oracle.build()
-    wl = workload_for(args.workload)
+    wl = workload_for(args.workload or HEADLINE)
     threads = os.cpu_count() or 1
     # each step: `threads` segments of the workload (truncated to sample_len
     # keys) sorted in parallel; the sample is sized so the run stays short
@@ -313,52 +317,56 @@ def run_reference(args, ws, rank):
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_ours(args, ws, rank, local):
+TORCH_VIEW_NAMES = {"f16": "int16", "bf16": "int16", "f32": "int32", "f64": "int64", "u32": "int32", "i32": "int32"}
+NUMPY_SIGNED = {"f16": np.int16, "bf16": np.int16, "f32": np.int32, "f64": np.int64, "u32": np.int32,
+                "i32": np.int32}
+# every workload of a default run (5: not_guaranteed + unsorted, 5det: gpu_to_gpu + stable_sorted);
+# the headline is the largest configuration in its deterministic mode
+ALL_WORKLOADS = ["1", "2", "3", "4", "5", "5det"]
+HEADLINE = "5det"
+
+
+class Resident:
+    """A workload's inputs in HBM, rotated over enough copies that one
+    rotation exceeds 3 x L2 (every step reads from HBM, not L2)."""
+
+    def __init__(self, wl, dev, l2):
+        import torch
+        self.wl = wl
+        keys_np = np.ascontiguousarray(wl.keys).view(NUMPY_SIGNED[wl.dtype])
+        self.key_bytes = keys_np.nbytes
+        self.copies = max(2, -(-3 * l2 // max(self.key_bytes, 1)))
+        self.keys = [torch.from_numpy(keys_np).to(dev) for _ in range(self.copies)]
+        self.vals = [torch.from_numpy(wl.values).to(dev) for _ in range(self.copies)] \
+            if wl.values is not None else None
+        self.offs = torch.from_numpy(wl.offsets).to(dev)
+        tv = getattr(torch, TORCH_VIEW_NAMES[wl.dtype])
+        self.out_k = torch.empty(wl.num_segments * wl.k, dtype=tv, device=dev)
+        self.out_v = torch.empty(wl.num_segments * wl.k, dtype=torch.int32, device=dev) \
+            if wl.values is not None else None
+
+    def call(self, i, lib=None):
+        import segmented_radix_top_gb300 as st
+        wl = self.wl
+        st.batched_topk(self.keys[i % self.copies], self.offs, wl.k,
+                        values=self.vals[i % self.copies] if self.vals else None, key_dtype=wl.dtype,
+                        direction=wl.direction, determinism=wl.determinism, tie_break=wl.tie_break,
+                        ordering=wl.ordering, out_keys=self.out_k, out_values=self.out_v,
+                        max_segment_len=wl.max_segment_len, lib=lib)
+
+
+def time_device(res, steps, warmup, dev, ws):
+    """Seconds per step over `steps` graph-replayed calls (CUDA events on the
+    replay stream, a barrier and a synchronize on both sides, max over
+    ranks), the launches per call, and the clocks sampled meanwhile."""
     import torch
     import segmented_radix_top_gb300 as st
-    from segmented_radix_top_gb300 import workloads as W
-
-    TORCH_VIEW = {"f16": torch.int16, "bf16": torch.int16, "f32": torch.int32, "f64": torch.int64,
-                  "u32": torch.int32, "i32": torch.int32}
-    NUMPY_SIGNED = {"f16": np.int16, "bf16": np.int16, "f32": np.int32, "f64": np.int64,
-                    "u32": np.int32, "i32": np.int32}
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    st.build()
-    wl = workload_for(args.workload)
-    props = torch.cuda.get_device_properties(dev)
-    l2 = int(getattr(props, "L2_cache_size", 0) or L2_FALLBACK)
-
-    keys_np = np.ascontiguousarray(wl.keys).view(NUMPY_SIGNED[wl.dtype])
-    key_bytes = keys_np.nbytes
-    copies = max(2, -(-3 * l2 // key_bytes))  # inputs of one rotation exceed 3x L2
-    keys_d = [torch.from_numpy(keys_np).to(dev) for _ in range(copies)]
-    vals_d = [torch.from_numpy(wl.values).to(dev) for _ in range(copies)] if wl.values is not None else None
-    offs_d = torch.from_numpy(wl.offsets).to(dev)
-    S, k = wl.num_segments, wl.k
-    out_k = torch.empty(S * k, dtype=TORCH_VIEW[wl.dtype], device=dev)
-    out_v = torch.empty(S * k, dtype=torch.int32, device=dev) if wl.values is not None else None
-    ml = wl.max_segment_len
-    n_keys = int(wl.lengths.sum())
-
-    def call(i):
-        st.batched_topk(keys_d[i % copies], offs_d, k, values=vals_d[i % copies] if vals_d else None,
-                        key_dtype=wl.dtype, direction=wl.direction, determinism=wl.determinism,
-                        tie_break=wl.tie_break, ordering=wl.ordering, out_keys=out_k,
-                        out_values=out_v, max_segment_len=ml)
-
-    # warm-up (eager): plans the launch, raises the shared-memory opt-in
-    for i in range(max(args.warmup, 1)):
-        call(i)
+    for i in range(max(warmup, 1)):  # eager: plans the launch, raises the shared-memory opt-in
+        res.call(i)
     torch.cuda.synchronize(dev)
-    launches_per_step = st.last_launch_count()
+    launches = st.last_launch_count()
     assert st.read_device_error() == 0
-
-    # CUDA graphs of G consecutive steps (rotating over the input copies)
-    G = max(1, min(args.steps, 64))
+    G = max(1, min(steps, 64))
     s = torch.cuda.Stream(dev)
     graphs = {}
 
@@ -367,11 +375,11 @@ def run_ours(args, ws, rank, local):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=s):
                 for i in range(n):
-                    call(i)
+                    res.call(i)
             graphs[n] = g
         return graphs[n]
 
-    full, rem = divmod(args.steps, G)
+    full, rem = divmod(steps, G)
     plan = [G] * full + ([rem] if rem else [])
     for n in set(plan):
         graph_for(n).replay()
@@ -380,14 +388,13 @@ def run_ours(args, ws, rank, local):
         for n in plan[:2]:
             graphs[n].replay()
     torch.cuda.synchronize(dev)
-
     cur = torch.cuda.current_stream(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev.index) as clk:
         e0.record(cur)
         for n in plan:
             graphs[n].replay()
@@ -397,28 +404,31 @@ def run_ours(args, ws, rank, local):
         import torch.distributed as dist
         dist.barrier()
     el = e0.elapsed_time(e1) / 1e3
-    el_max = reduce_max(el, ws, dev)
-    step_s = el_max / args.steps
-    # device time of one step: one launch, or the warp-path launch for short
-    # segments plus the CTA launch for the rest (their bytes are counted together)
-    kernel_s = el / args.steps
     assert st.read_device_error() == 0
+    return reduce_max(el, ws, dev) / steps, el / steps, launches, clk.summary(), G
 
-    # end to end through the host-buffer entry point (pinned host memory)
+
+def time_e2e(wl, steps, dev, ws):
+    """Keys per second through segtopk_batched_topk_host from pinned host
+    buffers (host<->device copies inside the timed region), and the bytes
+    copied per step."""
+    import torch
+    import segmented_radix_top_gb300 as st
+    keys_np = np.ascontiguousarray(wl.keys).view(NUMPY_SIGNED[wl.dtype])
+    tv = getattr(torch, TORCH_VIEW_NAMES[wl.dtype])
     h_keys = torch.from_numpy(keys_np).pin_memory()
     h_vals = torch.from_numpy(wl.values).pin_memory() if wl.values is not None else None
     h_offs = torch.from_numpy(wl.offsets).pin_memory()
-    h_ok = torch.empty(S * k, dtype=TORCH_VIEW[wl.dtype]).pin_memory()
+    S, k = wl.num_segments, wl.k
+    h_ok = torch.empty(S * k, dtype=tv).pin_memory()
     h_ov = torch.empty(S * k, dtype=torch.int32).pin_memory() if h_vals is not None else None
-    ws_bytes = st.host_workspace_bytes(wl.dtype, h_vals is not None, wl.num_keys, S, k)
-    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    e2e_steps = max(1, min(args.steps, 30))
+    workspace = torch.empty(st.host_workspace_bytes(wl.dtype, h_vals is not None, wl.num_keys, S, k),
+                            dtype=torch.uint8, device=dev)
 
     def host_call():
-        st.batched_topk_host(wl.dtype, h_keys, h_offs, k, workspace, values=h_vals,
-                             direction=wl.direction, determinism=wl.determinism,
-                             tie_break=wl.tie_break, ordering=wl.ordering, out_keys=h_ok,
-                             out_values=h_ov, max_segment_len=ml)
+        st.batched_topk_host(wl.dtype, h_keys, h_offs, k, workspace, values=h_vals, direction=wl.direction,
+                             determinism=wl.determinism, tie_break=wl.tie_break, ordering=wl.ordering,
+                             out_keys=h_ok, out_values=h_ov, max_segment_len=wl.max_segment_len)
 
     for _ in range(2):
         host_call()
@@ -427,61 +437,146 @@ def run_ours(args, ws, rank, local):
         import torch.distributed as dist
         dist.barrier()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
+    for _ in range(steps):
         host_call()
     torch.cuda.synchronize(dev)
-    e2e_el = reduce_max(time.perf_counter() - t0, ws, dev)
-    h2d = h_keys.numel() * h_keys.element_size() + h_offs.numel() * 8 + \
-        h_ok.numel() * h_ok.element_size()
+    el = reduce_max(time.perf_counter() - t0, ws, dev)
+    # keys, offsets and the output slots go to the device; keys and, for
+    # pairs, the selected source indices come back (values stay on the host)
+    h2d = h_keys.numel() * h_keys.element_size() + h_offs.numel() * 8 + h_ok.numel() * h_ok.element_size()
     d2h = h_ok.numel() * h_ok.element_size()
     if h_vals is not None:
-        h2d += h_vals.numel() * 4 + h_ov.numel() * 4
+        h2d += h_ov.numel() * 4
         d2h += h_ov.numel() * 4
+    del workspace
+    return ws * int(wl.lengths.sum()) * steps / el, h2d, d2h, steps
 
-    if rank != 0:
-        return 0
+
+def config_line(name, wl, step_s, kernel_s, launches, clocks, G, copies, key_bytes, l2, sms, ws, steps):
     peak, peak_note = measured_peak()
     alg = algorithmic_bytes(wl)
     achieved = alg / kernel_s / 1e9
-    cpu_value, cpu_desc = oracle_keys_per_s(wl, seconds=10.0, threads=os.cpu_count() or 1)
-    workload_key = args.workload
+    n_keys = int(wl.lengths.sum())
+    return {
+        "workload": wl.name, "dtype": wl.dtype, "segments": wl.num_segments, "keys": n_keys, "k": wl.k,
+        "direction": wl.direction, "determinism": wl.determinism, "tie_break": wl.tie_break,
+        "ordering": wl.ordering, "pairs": wl.values is not None,
+        "us_per_step": step_s * 1e6,
+        "keys_per_s": ws * n_keys / step_s,
+        "segments_per_s": ws * wl.num_segments / step_s,
+        "hbm_gbs": achieved,
+        "formula_gbs": formula_bytes(wl) / kernel_s / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_note": peak_note,
+                     "traffic": profiled_traffic(name),
+                     "algorithmic_bytes_per_launch": alg, "launches_per_step": launches,
+                     "kernel": kernel_label(wl, launches, sms)},
+        "gpu_launches": steps * launches,
+        "l2": "inputs rotate over %d copies (%.0f MB of keys) > L2 %.0f MB" % (copies, copies * key_bytes / 1e6,
+                                                                             l2 / 1e6),
+        "timing": "CUDA graphs of %d calls, CUDA events on the replay stream" % G,
+        "clocks": clocks,
+    }
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import segmented_radix_top_gb300 as st
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    st.build()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or L2_FALLBACK)
+    names = [args.workload] if args.workload else ALL_WORKLOADS
+    headline = args.workload or HEADLINE
+    per = {}
+    head = None
+    for name in names:
+        wl = workload_for(name)
+        res = Resident(wl, dev, l2)
+        step_s, kernel_s, launches, clocks, G = time_device(res, args.steps, args.warmup, dev, ws)
+        line = config_line(name, wl, step_s, kernel_s, launches, clocks, G, res.copies, res.key_bytes, l2,
+                           props.multi_processor_count, ws, args.steps)
+        del res
+        torch.cuda.empty_cache()
+        e2e_steps = max(1, min(args.steps, 10 if name == headline else 3))
+        e2e_v, h2d, d2h, e2e_n = time_e2e(wl, e2e_steps, dev, ws)
+        line["e2e"] = {"value": e2e_v, "unit": "keys/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "steps": e2e_n}
+        torch.cuda.empty_cache()
+        per[name] = line
+        if name == headline:
+            head = (wl, line)
+    if rank != 0:
+        return 0
+    wl, hl = head
+    threads = os.cpu_count() or 1
+    cpu_value, cpu_desc = oracle_keys_per_s(wl, seconds=8.0, threads=threads)
+    cpu_single, _ = oracle_keys_per_s(wl, seconds=6.0, threads=1)
     line = {
         "metric": METRIC,
-        "value": ws * n_keys / step_s,
+        "value": hl["keys_per_s"],
         "unit": "keys/s",
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": step_s * 1e3,
+        "ms_per_step": hl["us_per_step"] / 1e3,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded PCG64 generators, segmented_radix_top_gb300/workloads.py)",
-        "config": {"workload": wl.name, "segments": S, "keys": n_keys, "k": k,
-                   "direction": wl.direction, "determinism": wl.determinism,
-                   "tie_break": wl.tie_break, "ordering": wl.ordering,
-                   "pairs": wl.values is not None,
-                   "l2": "inputs rotate over %d copies (%.0f MB of keys) > L2 %.0f MB" % (
-                       copies, copies * key_bytes / 1e6, l2 / 1e6),
-                   "timing": "CUDA graphs of %d calls, CUDA events on the replay stream" % G},
-        "segments_per_s": ws * S / step_s,
-        "hbm_gbs": alg / kernel_s / 1e9,
-        "formula_gbs": formula_bytes(wl) / kernel_s / 1e9,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_note": peak_note,
-                     "traffic": profiled_traffic(workload_key),
-                     "algorithmic_bytes_per_launch": alg,
-                     "launches_per_step": launches_per_step,
-                     "kernel": kernel_label(wl, launches_per_step, props.multi_processor_count)},
-        "cpu_baseline": {"value": cpu_value, "unit": "keys/s", "cores": os.cpu_count() or 1,
-                         "kind": "oracle", "sample": cpu_desc},
-        "e2e": {"value": ws * n_keys * e2e_steps / e2e_el, "unit": "keys/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps * launches_per_step,
-        "clocks": clk.summary(),
+        "config": {"workload": wl.name, "segments": wl.num_segments, "keys": hl["keys"], "k": wl.k,
+                   "direction": wl.direction, "determinism": wl.determinism, "tie_break": wl.tie_break,
+                   "ordering": wl.ordering, "pairs": wl.values is not None, "l2": hl["l2"],
+                   "timing": hl["timing"]},
+        "segments_per_s": hl["segments_per_s"],
+        "hbm_gbs": hl["hbm_gbs"],
+        "formula_gbs": hl["formula_gbs"],
+        "roofline": hl["roofline"],
+        "cpu_baseline": {"value": cpu_value, "unit": "keys/s", "cores": threads, "kind": "oracle",
+                         "sample": cpu_desc, "single_thread_value": cpu_single},
+        "e2e": hl["e2e"],
+        "gpu_launches": hl["gpu_launches"],
+        "clocks": hl["clocks"],
+        "per_config": {n: {k: v for k, v in d.items() if k not in ("clocks",)} | {"sm_mhz": d["clocks"]["sm_mhz"]}
+                       for n, d in per.items()},
     }
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_stats(args):
+    """Per-CTA counters of the segment kernel (instrumented build) for each
+    workload: one call after warm-up, summed over the launch's CTAs and
+    averaged per CTA. Prints one JSON line."""
+    import torch
+    import segmented_radix_top_gb300 as st
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L = st.load_instrumented()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or L2_FALLBACK)
+    out = {}
+    for name in ([args.workload] if args.workload else ALL_WORKLOADS):
+        wl = workload_for(name)
+        res = Resident(wl, dev, l2)
+        for i in range(3):
+            res.call(i, lib=L)
+        torch.cuda.synchronize(dev)
+        st.read_stats()
+        res.call(0, lib=L)
+        s = st.read_stats()
+        ctas = max(s["ctas"], 1)
+        per_cta = {k: round(v / ctas, 1) for k, v in s.items() if k != "ctas"}
+        out[name] = {"workload": wl.name, "ctas": s["ctas"], "per_cta": per_cta}
+        assert st.read_device_error(lib=L) == 0
+        del res
+        torch.cuda.empty_cache()
+    print(json.dumps({"stats": out, "build": "libsegtopk_instr.so (SEGTOPK_STATS)"}), flush=True)
     return 0
 
 
@@ -491,11 +586,16 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="2", choices=["1", "2", "3", "4", "5", "5det"])
+    ap.add_argument("--workload", default=None, choices=ALL_WORKLOADS,
+                    help="time one workload only (default: all, workload 5 deterministic as the headline)")
+    ap.add_argument("--stats", action="store_true",
+                    help="print per-CTA counters of the instrumented build instead of timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_setup()
+    if args.stats:
+        return run_stats(args) if rank == 0 else 0
     if args.impl == "reference":
         return run_reference(args, ws, rank)
     return run_ours(args, ws, rank, local)

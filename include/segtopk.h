@@ -27,6 +27,14 @@
 extern "C" {
 #endif
 
+/* Exported entry points (the library is built with hidden visibility, so
+ * that nothing else it contains can collide with another library's). */
+#if defined(__GNUC__)
+#define SEGTOPK_API __attribute__((visibility("default")))
+#else
+#define SEGTOPK_API
+#endif
+
 /* Key element types. Keys are read as raw bit patterns of this width. */
 typedef enum {
   SEGTOPK_F16 = 0,  /* IEEE binary16 */
@@ -76,7 +84,7 @@ typedef enum {
   SEGTOPK_ERROR_INVALID_VALUE = 1,       /* bad enum, null pointer, negative size, k < 0 */
   SEGTOPK_ERROR_INVALID_COMBINATION = 2, /* determinism / tie_break pair not allowed */
   SEGTOPK_ERROR_NOT_SUPPORTED = 3,       /* size or k outside this library's limits */
-  SEGTOPK_ERROR_MISALIGNED = 4,          /* keys pointer not 16-byte aligned */
+  SEGTOPK_ERROR_MISALIGNED = 4,          /* keys pointer not aligned to its element size */
   SEGTOPK_ERROR_CUDA = 5,                /* a CUDA runtime call failed: see segtopk_last_cuda_error */
   SEGTOPK_ERROR_DEVICE = 6               /* current device is not an sm_103 GPU */
 } segtopk_status;
@@ -101,10 +109,12 @@ typedef enum {
  *   key_dtype        element type of keys and out_keys.
  *   keys             key array; segment s covers elements
  *                    [segment_offsets[s], segment_offsets[s+1]). Must be
- *                    16-byte aligned. Read only.
+ *                    aligned to its element size (any element of a larger
+ *                    array may start it). Read only.
  *   values           optional int32 payload parallel to keys (NULL: keys only).
- *   segment_offsets  int64 array of num_segments + 1 element offsets. A
- *                    segment whose end is not greater than its begin is empty.
+ *   segment_offsets  int64 array of num_segments + 1 element offsets, each
+ *                    non-negative and within the key array. A segment whose
+ *                    end is not greater than its begin is empty.
  *   num_segments     number of segments (>= 0).
  *   k                items to select per segment (>= 0).
  *   direction, determinism, tie_break, ordering: see the enums. Valid
@@ -133,7 +143,7 @@ typedef enum {
  * gives the cudaError_t). The call does not synchronise (except as noted
  * for max_segment_len < 0).
  */
-int segtopk_batched_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+SEGTOPK_API int segtopk_batched_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
                          const int64_t* segment_offsets, int64_t num_segments, int32_t k,
                          segtopk_direction direction, segtopk_determinism determinism,
                          segtopk_tie_break tie_break, segtopk_ordering ordering, void* out_keys,
@@ -172,7 +182,7 @@ typedef struct {
  * requested width. Without options (and in segtopk_batched_topk), the
  * warp-select paths take the segments their default limits give when
  * k <= 32; the others take one CTA or cluster each. */
-int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+SEGTOPK_API int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
                             const int64_t* segment_offsets, int64_t num_segments, int32_t k,
                             segtopk_direction direction, segtopk_determinism determinism,
                             segtopk_tie_break tie_break, segtopk_ordering ordering, void* out_keys,
@@ -183,12 +193,20 @@ int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys, const int
  * Same operation with HOST buffers: keys, values, segment_offsets, out_keys
  * and out_values are host pointers (pinned memory gives full copy
  * bandwidth). The caller also passes a device workspace of at least
- * segtopk_host_workspace_bytes(...) bytes (the library allocates nothing).
- * The call copies the inputs to the device, runs segtopk_batched_topk on
- * `stream`, copies the results back and waits for the stream before
- * returning (so the host outputs are ready on return).
+ * segtopk_host_workspace_bytes(...) bytes, 256-byte aligned (the library
+ * allocates nothing). The call copies the keys, the offsets and the output
+ * slots to the device, runs the selection on `stream` (for pairs the kernel
+ * writes each selected element's source index), copies the results back,
+ * waits for the stream, and then gathers the selected values from the
+ * caller's host `values` array, so that only the keys cross to the device.
+ * The host outputs are ready on return.
+ *
+ * The host offsets are read on the host: every offset must be non-negative
+ * (SEGTOPK_ERROR_INVALID_VALUE otherwise, before anything is copied or
+ * launched), and max_segment_len is ignored (the true longest segment is
+ * known). Slots past a short segment's length keep their host contents.
  */
-int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+SEGTOPK_API int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
                               const int64_t* segment_offsets, int64_t num_segments, int32_t k,
                               segtopk_direction direction, segtopk_determinism determinism,
                               segtopk_tie_break tie_break, segtopk_ordering ordering,
@@ -198,8 +216,8 @@ int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* keys, const i
 /*
  * Size of the fixed device staging area of segtopk_batched_topk_host_noalloc:
  * 32 MiB. A request fits when segtopk_host_workspace_bytes(...) for its
- * sizes is at most this (for example about 4 million fp32 keys with int32
- * values, or 8 million fp32 keys alone).
+ * sizes is at most this (for example about 8 million fp32 keys, with or
+ * without int32 values: values stay on the host).
  */
 #define SEGTOPK_NOALLOC_STAGING_BYTES (32u * 1024u * 1024u)
 
@@ -219,7 +237,8 @@ int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* keys, const i
  *
  * Set-up: the first call on a device (with that device current) looks up the
  * array's device address once; make that first call before any stream
- * capture begins on the device.
+ * capture begins on the device. The address is kept for the life of the
+ * process: a device reset (cudaDeviceReset) between calls is not supported.
  *
  * Limits and errors: a request needing more than SEGTOPK_NOALLOC_STAGING_BYTES
  * of staging returns SEGTOPK_ERROR_NOT_SUPPORTED before anything is copied.
@@ -233,7 +252,7 @@ int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* keys, const i
  * Like segtopk_batched_topk_host, the call waits for `stream` before it
  * returns.
  */
-int segtopk_batched_topk_host_noalloc(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+SEGTOPK_API int segtopk_batched_topk_host_noalloc(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
                                       const int64_t* segment_offsets, int64_t num_segments, int32_t k,
                                       segtopk_direction direction, segtopk_determinism determinism,
                                       segtopk_tie_break tie_break, segtopk_ordering ordering,
@@ -242,15 +261,17 @@ int segtopk_batched_topk_host_noalloc(segtopk_dtype key_dtype, const void* keys,
 
 /* Device workspace bytes segtopk_batched_topk_host needs for these sizes
  * (num_keys = number of key elements the offsets address, i.e. the largest
- * segment end). Host-only arithmetic. */
-size_t segtopk_host_workspace_bytes(segtopk_dtype key_dtype, int has_values, int64_t num_keys,
+ * segment end): keys, offsets, output keys and, for pairs, the selected
+ * source indices. Host-only arithmetic; 0 for negative or oversized
+ * arguments. */
+SEGTOPK_API size_t segtopk_host_workspace_bytes(segtopk_dtype key_dtype, int has_values, int64_t num_keys,
                                     int64_t num_segments, int32_t k);
 
 /* Human-readable text of a status code (static storage). */
-const char* segtopk_status_string(int status);
+SEGTOPK_API const char* segtopk_status_string(int status);
 
 /* cudaError_t of the last SEGTOPK_ERROR_CUDA on the calling thread (0 if none). */
-int segtopk_last_cuda_error(void);
+SEGTOPK_API int segtopk_last_cuda_error(void);
 
 /*
  * Reads and clears the device-side error word of the current device. The
@@ -259,10 +280,36 @@ int segtopk_last_cuda_error(void);
  * the launch was planned for). Synchronises the device. Returns a status;
  * the word is stored in *error_word.
  */
-int segtopk_read_device_error(uint32_t* error_word);
+SEGTOPK_API int segtopk_read_device_error(uint32_t* error_word);
 
 /* Number of kernel launches the last successful call on this thread made. */
-int segtopk_last_launch_count(void);
+SEGTOPK_API int segtopk_last_launch_count(void);
+
+/*
+ * Diagnostics of the instrumented build (the library compiled with
+ * SEGTOPK_STATS and SEGTOPK_TEST_HOOKS, a separate shared object); the
+ * ordinary build returns SEGTOPK_ERROR_NOT_SUPPORTED from both and changes
+ * nothing. The source pages have no counterpart of either.
+ *
+ * segtopk_read_stats: synchronises the device, then sums and clears the
+ * per-CTA counters of the segment kernel over every launch since the last
+ * read: out[0] CTAs, [1] cycles, [2] cycles to the first bound, [3] cycles
+ * of the free-running stream, [4] cycles after it (final selection, merge,
+ * output), [5] ring chunks, [6] list trims, [7] slices read twice, [8] list
+ * entries at the end of the stream, [9] slices with a sampled first bound,
+ * [10] digit-selection passes, [11] cycles warp 0 waited for copies, [12]
+ * keys, [13] chunk shares of warp 0 that held candidates; n entries are
+ * written (zeros past 15).
+ *
+ * segtopk_set_test_hooks: the bound (SM clock cycles) after which a wait on
+ * a bulk copy gives up, and a number of bytes (a multiple of 16, at most
+ * 4096) added to the expected byte count of every slice's first copy, so
+ * that its wait runs out: tests of the bounded wait use it. The kernel then
+ * sets bit 0 of the device error word, writes no output for the affected
+ * segments and returns.
+ */
+SEGTOPK_API int segtopk_read_stats(uint64_t* out, int n);
+SEGTOPK_API int segtopk_set_test_hooks(long long wait_limit_cycles, uint32_t first_copy_extra_bytes);
 
 #ifdef __cplusplus
 }

@@ -8,7 +8,8 @@ that ABI (see _binding.py) and provides the seeded synthetic workloads
 from ._binding import (DETERMINISM, DIRECTION, DTYPE, KEY_BYTES, MAX_K, NOALLOC_STAGING_BYTES,  # noqa: F401
                        ORDERING, TIE_BREAK, SegTopKError, batched_topk, batched_topk_host,
                        batched_topk_host_noalloc, host_workspace_bytes,
-                       last_launch_count, library_path, load, read_device_error)
+                       last_launch_count, library_path, load, load_instrumented, read_device_error,
+                       read_stats, set_test_hooks)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

@@ -44,6 +44,10 @@ class Options(ctypes.Structure):
 
 
 _lib = None
+_instr = None
+STAT_NAMES = ["ctas", "cycles", "first_bound_cycles", "stream_cycles", "final_cycles", "chunks", "trims",
+              "restreams", "list_entries", "sampled_bounds", "digit_passes", "wait_cycles_warp0", "keys",
+              "candidate_shares_warp0"]
 
 
 def library_path() -> str:
@@ -55,10 +59,23 @@ def load():
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.LIB_PATH
+    _lib = _open(_build.LIB_PATH)
+    return _lib
+
+
+def load_instrumented():
+    """Load the instrumented build (statistics counters and test hooks),
+    building it first if needed. Its calls are the same as load()'s."""
+    global _instr
+    if _instr is None:
+        _instr = _open(_build.build(variant="instr"))
+    return _instr
+
+
+def _open(path):
     if not os.path.exists(path):
-        raise RuntimeError("libsegtopk.so is not built (run __graft_entry__.build()); "
-                           "there is no fallback implementation")
+        raise RuntimeError("%s is not built (run __graft_entry__.build()); "
+                           "there is no fallback implementation" % os.path.basename(path))
     L = ctypes.CDLL(path)
     c_int, c_i32, c_i64, vp = ctypes.c_int, ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
     L.segtopk_batched_topk.restype = c_int
@@ -83,13 +100,16 @@ def load():
     L.segtopk_last_launch_count.argtypes = []
     L.segtopk_read_device_error.restype = c_int
     L.segtopk_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
-    _lib = L
+    L.segtopk_read_stats.restype = c_int
+    L.segtopk_read_stats.argtypes = [ctypes.POINTER(ctypes.c_uint64), c_int]
+    L.segtopk_set_test_hooks.restype = c_int
+    L.segtopk_set_test_hooks.argtypes = [ctypes.c_longlong, ctypes.c_uint32]
     return L
 
 
-def _check(rc: int):
+def _check(rc: int, lib=None):
     if rc != 0:
-        L = load()
+        L = lib if lib is not None else load()
         msg = L.segtopk_status_string(rc).decode()
         if rc == 5:
             msg += " (cudaError %d)" % L.segtopk_last_cuda_error()
@@ -121,11 +141,12 @@ def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, v
                  tie_break: str = "prefer_smaller_index", ordering: str = "stable_sorted",
                  out_keys=None, out_values=None, max_segment_len: int | None = None,
                  key_dtype: str | None = None, stream=None, cluster_width: int = 0,
-                 small_segment_max_len: int = 0, team_segment_max_len: int = 0):
+                 small_segment_max_len: int = 0, team_segment_max_len: int = 0, lib=None):
     """Segmented top-k on the GPU through libsegtopk (see include/segtopk.h).
 
-    keys: 1-D CUDA tensor (16-byte aligned); its element size must match the
-    key type (a raw-bits tensor of the same width works with key_dtype).
+    keys: 1-D CUDA tensor (any view; its data pointer aligned to the element
+    size); its element size must match the key type (a raw-bits tensor of
+    the same width works with key_dtype).
     segment_offsets: int64 CUDA tensor of num_segments + 1 offsets.
     Returns (out_keys, out_values) of shape [num_segments * k]; out_values is
     None for keys-only calls. Slots past a short segment's length are left as
@@ -133,9 +154,10 @@ def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, v
     cluster_width forces the CTAs per segment (0: automatic);
     small_segment_max_len / team_segment_max_len set which segments take one
     warp / a team of eight warps each when k <= 32 (0: the defaults, or none
-    with a forced width; < 0: none).
+    with a forced width; < 0: none). `lib` selects another build of the
+    library (load_instrumented()).
     """
-    L = load()
+    L = lib if lib is not None else load()
     kd = key_dtype_of(keys, key_dtype)
     if segment_offsets.dtype != torch.int64:
         raise ValueError("segment_offsets must be int64")
@@ -154,7 +176,7 @@ def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, v
                                    DETERMINISM[determinism], TIE_BREAK[tie_break], ORDERING[ordering],
                                    _ptr(out_keys), _ptr(out_values), ml, ctypes.byref(opts),
                                    _stream_handle(stream, keys.device))
-    _check(rc)
+    _check(rc, L)
     return out_keys, out_values
 
 
@@ -215,11 +237,27 @@ def batched_topk_host_noalloc(key_dtype: str, keys: torch.Tensor, segment_offset
     return out_keys, out_values
 
 
-def read_device_error() -> int:
+def read_device_error(lib=None) -> int:
     """Reads and clears the kernels' device error word (synchronises)."""
     w = ctypes.c_uint32(0)
-    _check(load().segtopk_read_device_error(ctypes.byref(w)))
+    L = lib if lib is not None else load()
+    _check(L.segtopk_read_device_error(ctypes.byref(w)), L)
     return int(w.value)
+
+
+def read_stats() -> dict:
+    """Sums and clears the instrumented build's per-CTA counters (synchronises)."""
+    L = load_instrumented()
+    arr = (ctypes.c_uint64 * 16)()
+    _check(L.segtopk_read_stats(arr, 16), L)
+    return {name: int(arr[i]) for i, name in enumerate(STAT_NAMES)}
+
+
+def set_test_hooks(wait_limit_cycles: int, first_copy_extra_bytes: int = 0):
+    """Instrumented build only: the copy-wait bound and the bytes added to
+    every slice's first copy's expected count (see include/segtopk.h)."""
+    L = load_instrumented()
+    _check(L.segtopk_set_test_hooks(int(wait_limit_cycles), int(first_copy_extra_bytes)), L)
 
 
 def last_launch_count() -> int:

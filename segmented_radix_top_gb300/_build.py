@@ -3,6 +3,11 @@
 Each .cu is compiled to an object in parallel, then linked into one shared
 library next to this file. A rebuild happens only when a source or header is
 newer than the library.
+
+The instrumented variant (libsegtopk_instr.so, variant="instr") is the same
+sources compiled with SEGTOPK_STATS and SEGTOPK_TEST_HOOKS: per-CTA counters
+(segtopk_read_stats) and the test hooks of the bounded copy wait
+(segtopk_set_test_hooks). It is built only when asked for.
 """
 from __future__ import annotations
 
@@ -18,9 +23,18 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libsegtopk.so")
+VARIANTS = {
+    "": (BUILD_DIR, LIB_PATH, []),
+    "instr": (os.path.join(HERE, "_build_instr"), os.path.join(HERE, "libsegtopk_instr.so"),
+              ["-DSEGTOPK_STATS", "-DSEGTOPK_TEST_HOOKS"]),
+}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
+# hidden visibility: only the C ABI (SEGTOPK_API in include/segtopk.h) is
+# exported, so two builds loaded in one process (the ordinary and the
+# instrumented one) share no symbol, not even a function-local static
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
+              "-I", INCLUDE,
               "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
 
 
@@ -38,21 +52,27 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def lib_path(variant: str = "") -> str:
+    return VARIANTS[variant][1]
+
+
+def up_to_date(variant: str = "") -> bool:
+    path = lib_path(variant)
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = NVCC_FLAGS + list(extra_flags or [])
+def build(force: bool = False, verbose: bool = False, extra_flags=None, variant: str = "") -> str:
+    build_dir, out_path, variant_flags = VARIANTS[variant]
+    if not force and up_to_date(variant):
+        return out_path
+    os.makedirs(build_dir, exist_ok=True)
+    flags = NVCC_FLAGS + variant_flags + list(extra_flags or [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc()] + ARCH + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,15 +84,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB_PATH + ".tmp.%d" % os.getpid()
+    tmp = out_path + ".tmp.%d" % os.getpid()
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out_path)
+    return out_path
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
-                extra_flags=["-Xptxas", "-v"] if "-v" in sys.argv else None))
+                extra_flags=["-Xptxas", "-v"] if "-v" in sys.argv else None,
+                variant="instr" if "--instr" in sys.argv else ""))

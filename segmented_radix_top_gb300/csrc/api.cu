@@ -93,9 +93,17 @@ constexpr uint32_t kGatherMaxItems = 2048;
 // read) tightens the bound.
 uint32_t list_slack(uint32_t k) { return std::max(1024u, k / 2); }
 
-// Ring-stage and candidate-buffer bytes of a kernel profile.
-uint32_t profile_chunk_bytes(int profile) { return profile == 0 ? ProfileLong::kChunkBytes : ProfileMany::kChunkBytes; }
+// Ring bytes of a kernel profile (kStages stages).
+uint32_t profile_ring_bytes(int profile)
+{
+  return kStages * (profile == 0 ? ProfileLong::kChunkBytes : ProfileMany::kChunkBytes);
+}
 uint32_t profile_cand_bytes(int profile) { return profile == 0 ? ProfileLong::kCandBytes : ProfileMany::kCandBytes; }
+
+// Wait bound and copy-count offset handed to the kernels (changed only by the
+// test hooks of the instrumented build).
+long long g_wait_limit = kWaitLimitCycles;
+uint32_t g_test_extra_tx = 0;
 
 // Shared-memory sizing for a given k, cluster width and kernel profile. The
 // ring doubles as sort scratch and, in a cluster leader, as gather space.
@@ -105,7 +113,7 @@ Plan size_plan(const KeyOps& ops, int32_t k, int cluster, int profile)
   const uint32_t kb = (uint32_t)ops.key_bytes;
   const uint32_t uk = (uint32_t)k;
   pl.list_cap = align_up(uk + list_slack(uk), 32);
-  const uint32_t stream_ring = kStages * profile_chunk_bytes(profile);
+  const uint32_t stream_ring = profile_ring_bytes(profile);
   const uint32_t sort_need = std::max(sort_scratch_bytes(uk, ops.rank_bits), finalize_scratch_bytes(kCountMax));
   uint32_t need = sort_need;
   pl.merge_gather = 0;
@@ -227,6 +235,16 @@ cudaError_t get_plan(int dtype, const KeyOps& ops, int64_t num_segments, int64_t
   return cudaSuccess;
 }
 
+int key_bytes_of(int dtype)
+{
+  switch (dtype) {
+  case SEGTOPK_F16:
+  case SEGTOPK_BF16: return 2;
+  case SEGTOPK_F64: return 8;
+  default: return 4;
+  }
+}
+
 bool valid_pair(int det, int tie)
 {
   if (tie == SEGTOPK_TIE_UNSPECIFIED)
@@ -236,7 +254,8 @@ bool valid_pair(int det, int tie)
 
 int validate(int dtype, const void* keys, const int32_t* values, const int64_t* offsets,
              int64_t num_segments, int32_t k, int direction, int determinism, int tie_break,
-             int ordering, const void* out_keys, const int32_t* out_values, int64_t max_len)
+             int ordering, const void* out_keys, const int32_t* out_values, int64_t max_len,
+             bool index_values = false)
 {
   if (dtype < SEGTOPK_F16 || dtype > SEGTOPK_I32)
     return SEGTOPK_ERROR_INVALID_VALUE;
@@ -254,9 +273,10 @@ int validate(int dtype, const void* keys, const int32_t* values, const int64_t* 
     return SEGTOPK_ERROR_INVALID_VALUE;
   if (num_segments == 0 || k == 0)
     return SEGTOPK_SUCCESS;
-  if (!keys || !offsets || !out_keys || (values && !out_values) || (!values && out_values))
+  // out_values without values: only the host-buffer path's index mode
+  if (!keys || !offsets || !out_keys || (values && !out_values) || (!values && out_values && !index_values))
     return SEGTOPK_ERROR_INVALID_VALUE;
-  if (((uintptr_t)keys & 15u) != 0)
+  if (((uintptr_t)keys % (uintptr_t)key_bytes_of(dtype)) != 0)
     return SEGTOPK_ERROR_MISALIGNED;
   if (max_len > SEGTOPK_MAX_SEGMENT_LEN)
     return SEGTOPK_ERROR_NOT_SUPPORTED;
@@ -267,22 +287,14 @@ int validate(int dtype, const void* keys, const int32_t* values, const int64_t* 
   return -1; // proceed
 }
 
-} // namespace
-
-// Records a failed CUDA call for segtopk_last_cuda_error on this thread (for
-// the library's other translation units); returns SEGTOPK_ERROR_CUDA.
-int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
-
-} // namespace segtopk
-
-using namespace segtopk;
-
-extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
-                                       const int64_t* segment_offsets, int64_t num_segments, int32_t k,
-                                       segtopk_direction direction, segtopk_determinism determinism,
-                                       segtopk_tie_break tie_break, segtopk_ordering ordering,
-                                       void* out_keys, int32_t* out_values, int64_t max_segment_len,
-                                       const segtopk_options* options, void* stream)
+// The device-buffer call. With index_values, values may be null while
+// out_values is not: out_values then receives each selected element's
+// segment-local source index (the host-buffer path gathers the values
+// itself).
+int run_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values, const int64_t* segment_offsets,
+             int64_t num_segments, int32_t k, segtopk_direction direction, segtopk_determinism determinism,
+             segtopk_tie_break tie_break, segtopk_ordering ordering, void* out_keys, int32_t* out_values,
+             int64_t max_segment_len, const segtopk_options* options, void* stream, bool index_values)
 {
   t_last_launch_count = 0;
   int forced_width = 0;
@@ -298,7 +310,7 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
     team_max = options->team_segment_max_len;
   }
   int v = validate(key_dtype, keys, values, segment_offsets, num_segments, k, direction, determinism,
-                   tie_break, ordering, out_keys, out_values, max_segment_len);
+                   tie_break, ordering, out_keys, out_values, max_segment_len, index_values);
   if (v >= 0)
     return v;
   DeviceInfo dev;
@@ -417,6 +429,8 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
   p.spec_c = pl.waves <= 1 ? 3.0f : (p.spec_small ? 2.0f : 1.0f);
   p.ring_stages = kStages;
   p.ring_bytes = pl.ring_bytes;
+  p.wait_limit = g_wait_limit;
+  p.test_extra_tx = g_test_extra_tx;
   p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;
   p.sorted = (ordering != SEGTOPK_UNSORTED) ? 1 : 0;
   p.flag_overlong = 1;
@@ -425,6 +439,27 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
     return cuda_fail(e);
   t_last_launch_count = launches + 1;
   return SEGTOPK_SUCCESS;
+}
+
+} // namespace
+
+// Records a failed CUDA call for segtopk_last_cuda_error on this thread (for
+// the library's other translation units); returns SEGTOPK_ERROR_CUDA.
+int record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
+} // namespace segtopk
+
+using namespace segtopk;
+
+extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
+                                       const int64_t* segment_offsets, int64_t num_segments, int32_t k,
+                                       segtopk_direction direction, segtopk_determinism determinism,
+                                       segtopk_tie_break tie_break, segtopk_ordering ordering,
+                                       void* out_keys, int32_t* out_values, int64_t max_segment_len,
+                                       const segtopk_options* options, void* stream)
+{
+  return run_topk(key_dtype, keys, values, segment_offsets, num_segments, k, direction, determinism, tie_break,
+                  ordering, out_keys, out_values, max_segment_len, options, stream, false);
 }
 
 extern "C" int segtopk_batched_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
@@ -441,27 +476,39 @@ extern "C" int segtopk_batched_topk(segtopk_dtype key_dtype, const void* keys, c
 
 namespace {
 size_t ws_align(size_t x) { return (x + 255) & ~(size_t)255; }
-int key_bytes_of(int dtype)
-{
-  switch (dtype) {
-  case SEGTOPK_F16:
-  case SEGTOPK_BF16: return 2;
-  case SEGTOPK_F64: return 8;
-  default: return 4;
-  }
-}
 } // namespace
+
+namespace segtopk {
+int host_offsets_scan(const int64_t* offsets, int64_t num_segments, int64_t* num_keys, int64_t* max_len)
+{
+  int64_t nk = 0, ml = 0;
+  for (int64_t s = 0; s <= num_segments; ++s)
+    if (offsets[s] < 0)
+      return SEGTOPK_ERROR_INVALID_VALUE;
+  for (int64_t s = 0; s < num_segments; ++s) {
+    nk = std::max(nk, offsets[s + 1]);
+    ml = std::max(ml, offsets[s + 1] - offsets[s]);
+  }
+  if ((uint64_t)nk > (uint64_t)(SIZE_MAX / 16))
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  *num_keys = nk;
+  *max_len = ml;
+  return SEGTOPK_SUCCESS;
+}
+} // namespace segtopk
 
 extern "C" size_t segtopk_host_workspace_bytes(segtopk_dtype key_dtype, int has_values, int64_t num_keys,
                                                int64_t num_segments, int32_t k)
 {
-  if (num_keys < 0 || num_segments < 0 || k < 0)
+  if (num_keys < 0 || num_segments < 0 || k < 0 || (uint64_t)num_keys > (uint64_t)(SIZE_MAX / 16) ||
+      num_segments > (int64_t)0x7fffffff)
     return 0;
   const size_t kb = (size_t)key_bytes_of(key_dtype);
+  // keys, offsets, output keys and, for pairs, the selected source indices
   size_t b = ws_align((size_t)num_keys * kb) + ws_align((size_t)(num_segments + 1) * 8) +
              ws_align((size_t)num_segments * (size_t)k * kb);
   if (has_values)
-    b += ws_align((size_t)num_keys * 4) + ws_align((size_t)num_segments * (size_t)k * 4);
+    b += ws_align((size_t)num_segments * (size_t)k * 4);
   return b;
 }
 
@@ -473,68 +520,75 @@ extern "C" int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* ke
                                          void* device_workspace, size_t workspace_bytes, void* stream)
 {
   t_last_launch_count = 0;
+  (void)max_segment_len; // the host reads its own offsets: the true longest segment is known
   int v = validate(key_dtype, keys ? (const void*)16 : nullptr, values, segment_offsets, num_segments, k,
-                   direction, determinism, tie_break, ordering, out_keys, out_values, max_segment_len);
+                   direction, determinism, tie_break, ordering, out_keys, out_values, -1);
   if (v >= 0)
     return v;
   if (!device_workspace)
     return SEGTOPK_ERROR_INVALID_VALUE;
   if (((uintptr_t)device_workspace & 255u) != 0)
     return SEGTOPK_ERROR_MISALIGNED;
-  // keys addressed by the offsets: the host reads its own offsets array
   int64_t num_keys = 0, max_len = 0;
-  for (int64_t s = 0; s < num_segments; ++s) {
-    num_keys = std::max(num_keys, segment_offsets[s + 1]);
-    max_len = std::max(max_len, segment_offsets[s + 1] - segment_offsets[s]);
-  }
-  if (max_segment_len >= 0)
-    max_len = std::min(max_len, max_segment_len);
+  v = host_offsets_scan(segment_offsets, num_segments, &num_keys, &max_len);
+  if (v != SEGTOPK_SUCCESS)
+    return v;
   if (max_len > SEGTOPK_MAX_SEGMENT_LEN)
     return SEGTOPK_ERROR_NOT_SUPPORTED;
   const size_t need = segtopk_host_workspace_bytes(key_dtype, values != nullptr, num_keys, num_segments, k);
-  if (workspace_bytes < need)
+  if (need == 0 || workspace_bytes < need)
     return SEGTOPK_ERROR_INVALID_VALUE;
   const size_t kb = (size_t)key_bytes_of(key_dtype);
+  const size_t slots = (size_t)num_segments * (size_t)k;
   char* w = (char*)device_workspace;
   void* d_keys = w;
   w += ws_align((size_t)num_keys * kb);
   int64_t* d_offs = (int64_t*)w;
   w += ws_align((size_t)(num_segments + 1) * 8);
   void* d_out_keys = w;
-  w += ws_align((size_t)num_segments * (size_t)k * kb);
-  int32_t* d_values = nullptr;
-  int32_t* d_out_values = nullptr;
-  if (values) {
-    d_values = (int32_t*)w;
-    w += ws_align((size_t)num_keys * 4);
-    d_out_values = (int32_t*)w;
-  }
+  w += ws_align(slots * kb);
+  int32_t* d_out_idx = values ? (int32_t*)w : nullptr;
+  // Only keys and offsets travel to the device: the kernel writes each
+  // selected element's segment-local source index, and the values are
+  // gathered here from the caller's host array.
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaMemcpyAsync(d_keys, keys, (size_t)num_keys * kb, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(d_offs, segment_offsets, (size_t)(num_segments + 1) * 8, cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess && values)
-    e = cudaMemcpyAsync(d_values, values, (size_t)num_keys * 4, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess)
-    return cuda_fail(e);
   // slots past a short segment's length keep the caller's host contents
-  e = cudaMemcpyAsync(d_out_keys, out_keys, (size_t)num_segments * (size_t)k * kb, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(d_out_keys, out_keys, slots * kb, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess && values)
-    e = cudaMemcpyAsync(d_out_values, out_values, (size_t)num_segments * (size_t)k * 4, cudaMemcpyHostToDevice, st);
+    e = cudaMemcpyAsync(d_out_idx, out_values, slots * 4, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess)
     return cuda_fail(e);
-  int rc = segtopk_batched_topk(key_dtype, d_keys, d_values, d_offs, num_segments, k, direction, determinism,
-                                tie_break, ordering, d_out_keys, d_out_values, max_len, stream);
+  int rc = run_topk(key_dtype, d_keys, nullptr, d_offs, num_segments, k, direction, determinism, tie_break,
+                    ordering, d_out_keys, d_out_idx, max_len, nullptr, stream, true);
   if (rc != SEGTOPK_SUCCESS)
     return rc;
   const int launches = t_last_launch_count;
-  e = cudaMemcpyAsync(out_keys, d_out_keys, (size_t)num_segments * (size_t)k * kb, cudaMemcpyDeviceToHost, st);
+  e = cudaMemcpyAsync(out_keys, d_out_keys, slots * kb, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess && values)
-    e = cudaMemcpyAsync(out_values, d_out_values, (size_t)num_segments * (size_t)k * 4, cudaMemcpyDeviceToHost, st);
+    e = cudaMemcpyAsync(out_values, d_out_idx, slots * 4, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess)
     e = cudaStreamSynchronize(st);
   if (e != cudaSuccess)
     return cuda_fail(e);
+  if (values) {
+    // written slots hold source indices: replace them by the values
+    for (int64_t s = 0; s < num_segments; ++s) {
+      const int64_t b = segment_offsets[s];
+      const int64_t n = std::max<int64_t>(segment_offsets[s + 1] - b, 0);
+      const int64_t m = std::min<int64_t>(n, k);
+      int32_t* ov = out_values + (size_t)s * (size_t)k;
+      for (int64_t j = 0; j < m; ++j) {
+        const int64_t i = ov[j];
+        if (i < 0 || i >= n)
+          return SEGTOPK_ERROR_DEVICE; // cannot happen: the kernel writes indices of the segment
+        ov[j] = values[b + i];
+      }
+    }
+  }
   t_last_launch_count = launches;
   return SEGTOPK_SUCCESS;
 }
@@ -546,7 +600,7 @@ extern "C" const char* segtopk_status_string(int status)
   case SEGTOPK_ERROR_INVALID_VALUE: return "invalid argument value";
   case SEGTOPK_ERROR_INVALID_COMBINATION: return "determinism / tie_break combination not allowed";
   case SEGTOPK_ERROR_NOT_SUPPORTED: return "request outside the supported limits";
-  case SEGTOPK_ERROR_MISALIGNED: return "keys pointer is not 16-byte aligned";
+  case SEGTOPK_ERROR_MISALIGNED: return "keys pointer is not aligned to its element size";
   case SEGTOPK_ERROR_CUDA: return "CUDA runtime error";
   case SEGTOPK_ERROR_DEVICE: return "unsupported device (needs sm_103)";
   default: return "unknown status";
@@ -576,4 +630,43 @@ extern "C" int segtopk_read_device_error(uint32_t* error_word)
   }
   *error_word = all;
   return SEGTOPK_SUCCESS;
+}
+
+extern "C" int segtopk_read_stats(uint64_t* out, int n)
+{
+  if (!out || n < 0)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+#ifndef SEGTOPK_STATS
+  return SEGTOPK_ERROR_NOT_SUPPORTED;
+#else
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  unsigned long long sum[kStatCount] = {};
+  const KeyOps* list[] = {&key_ops_f16(), &key_ops_bf16(), &key_ops_f32(),
+                          &key_ops_f64(), &key_ops_u32(), &key_ops_i32()};
+  for (const KeyOps* o : list) {
+    e = o->read_stats(sum);
+    if (e != cudaSuccess)
+      return cuda_fail(e);
+  }
+  for (int i = 0; i < n; ++i)
+    out[i] = i < kStatCount ? (uint64_t)sum[i] : 0u;
+  return SEGTOPK_SUCCESS;
+#endif
+}
+
+extern "C" int segtopk_set_test_hooks(long long wait_limit_cycles, uint32_t first_copy_extra_bytes)
+{
+#ifndef SEGTOPK_TEST_HOOKS
+  (void)wait_limit_cycles;
+  (void)first_copy_extra_bytes;
+  return SEGTOPK_ERROR_NOT_SUPPORTED;
+#else
+  if (wait_limit_cycles <= 0 || (first_copy_extra_bytes & 15u) != 0 || first_copy_extra_bytes > 4096u)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  g_wait_limit = wait_limit_cycles;
+  g_test_extra_tx = first_copy_extra_bytes;
+  return SEGTOPK_SUCCESS;
+#endif
 }

@@ -56,6 +56,9 @@ struct Ctrl {
   uint32_t spec_kept;                // small speculative selection: sample keys kept
   uint64_t xb[16][2];                // cluster leader: every CTA's local k-th (rank, preference index)
   uint64_t xb_min[2];                // the cluster-wide minimum of xb
+  uint32_t abort;                    // a wait on a bulk copy gave up: the CTA writes no output
+  uint32_t pad_;
+  unsigned long long stat[16];       // per-CTA counters of the statistics build
 };
 static_assert(sizeof(PassSlot) % 16 == 0, "every slot's histogram is 16-byte aligned");
 static_assert(offsetof(Ctrl, slot) % 16 == 0, "the slots are 16-byte aligned");
@@ -1208,7 +1211,7 @@ __device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, cons
       if (p < m) {
         out_keys[p] = raw[i];
         if (out_values)
-          out_values[p] = values[idx[i]];
+          out_values[p] = value_at(values, idx[i]);
       }
     }
     return;
@@ -1227,7 +1230,7 @@ __device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, cons
     if (p < m) {
       out_keys[p] = raw[i];
       if (out_values)
-        out_values[p] = values[idx[i]];
+        out_values[p] = value_at(values, idx[i]);
     }
   }
 }
@@ -1274,7 +1277,7 @@ __device__ __forceinline__ void sort_write_ept(const typename TR::Raw* raw, cons
       const uint32_t slot = (uint32_t)b[r];
       out_keys[e] = raw[slot];
       if (out_values)
-        out_values[e] = values[idx[slot]];
+        out_values[e] = value_at(values, idx[slot]);
     }
   }
 }
@@ -1306,7 +1309,7 @@ __device__ __forceinline__ void sort_and_write(const typename TR::Raw* raw, cons
       const uint32_t s = pay[j];
       out_keys[j] = raw[s];
       if (out_values)
-        out_values[j] = values[idx[s]];
+        out_values[j] = value_at(values, idx[s]);
     }
   } else {
     uint64_t* khi = reinterpret_cast<uint64_t*>(scratch);
@@ -1321,7 +1324,7 @@ __device__ __forceinline__ void sort_and_write(const typename TR::Raw* raw, cons
       const uint32_t s = (uint32_t)klo[j];
       out_keys[j] = raw[s];
       if (out_values)
-        out_values[j] = values[idx[s]];
+        out_values[j] = value_at(values, idx[s]);
     }
   }
 }

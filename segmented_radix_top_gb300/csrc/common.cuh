@@ -69,15 +69,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
   return ok != 0;
 }
 
-// Bounded wait: gives up after about one second of SM clock cycles, records
-// the failure and lets the caller continue on a uniform control path.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity)
+// As mbar_try_wait, with the thread suspended for at most about `ns`
+// nanoseconds while the phase is incomplete (so that a polling loop around
+// it also notices other events soon).
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t ns)
+{
+  uint32_t ok;
+  asm volatile(
+    "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+    : "=r"(ok)
+    : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+    : "memory");
+  return ok != 0;
+}
+
+// Default bound of a wait on a bulk copy: about one second of SM clock cycles.
+constexpr long long kWaitLimitCycles = 1ll << 31;
+
+// Bounded wait on the phase of `bar` with the given parity: gives up after
+// `limit` SM clock cycles and records the failure in the device error word.
+// Callers make the outcome uniform (one waiting lane, broadcast) before
+// branching on it.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long long limit = kWaitLimitCycles)
 {
   if (mbar_try_wait(bar, parity))
     return true;
   const long long start = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > (1ll << 31)) {
+    if (clock64() - start > limit) {
       raise_error(kErrCopyTimeout);
       return false;
     }
@@ -184,21 +203,26 @@ __device__ __forceinline__ void dsmem_st(uint32_t addr, uint64_t v)
 // Each key kind provides
 //   rank(x, dirmask)       the rank code (smaller = better);
 //   unrank(r, dirmask)     raw bits of a key with rank r (never -0.0);
-//   may_pass(v, b, is_max) for a 16-byte vector of keys: false only if no
-//                          key in it can rank below the bound b (rank b.tau,
-//                          raw bits b.raw). It may answer true for keys that
-//                          then fail the exact rank test (ties, NaNs), never
+//   may_pass(v, braw, brank, is_max, strict)
+//                          for a 16-byte vector of keys: false only if no key
+//                          in it ranks below brank (strict) or at most brank
+//                          (not strict), where braw are the bits of a key
+//                          whose rank is brank. It may answer true for keys
+//                          that then fail the exact test (ties, NaNs), never
 //                          false for one that passes. Floats use one native
-//                          compare per key ("not worse than the bound", which
-//                          is also true for NaN), integers the exact test.
+//                          compare per key against braw ("better than" or
+//                          "not worse than", both also true for NaN);
+//                          integers the exact test on the rank.
 // ---------------------------------------------------------------------------
-enum class KeyKind : int { F16 = 0, BF16 = 1, F32 = 2, F64 = 3, U32 = 4, I32 = 5 };
-
+// A rank bound in both domains: a key enters iff its rank is below tau;
+// raw holds the bits of a key whose rank is tau (the raw-domain filter).
 template <class Raw, class Rank>
 struct Bound {
-  Rank tau; // accept a key iff its rank is below tau
-  Raw raw;  // bits of a key whose rank is tau
+  Rank tau;
+  Raw raw;
 };
+
+enum class KeyKind : int { F16 = 0, BF16 = 1, F32 = 2, F64 = 3, U32 = 4, I32 = 5 };
 
 template <KeyKind K>
 struct KeyTraits;
@@ -232,16 +256,18 @@ struct KeyTraits<KeyKind::F16> {
   {
     return FloatRank<uint16_t, 16>::t_inv((uint16_t)(r ^ dirmask));
   }
-  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  __device__ __forceinline__ static bool may_pass(const uint4& v, Raw braw, Rank, bool is_max, bool strict)
   {
-    const __half e = __ushort_as_half(b.raw);
+    const __half e = __ushort_as_half(braw);
     const __half2 h = __halves2half2(e, e);
     const __half2* w = reinterpret_cast<const __half2*>(&v);
     unsigned m;
     if (is_max)
-      m = __hgeu2_mask(w[0], h) | __hgeu2_mask(w[1], h) | __hgeu2_mask(w[2], h) | __hgeu2_mask(w[3], h);
+      m = strict ? (__hgtu2_mask(w[0], h) | __hgtu2_mask(w[1], h) | __hgtu2_mask(w[2], h) | __hgtu2_mask(w[3], h))
+                 : (__hgeu2_mask(w[0], h) | __hgeu2_mask(w[1], h) | __hgeu2_mask(w[2], h) | __hgeu2_mask(w[3], h));
     else
-      m = __hleu2_mask(w[0], h) | __hleu2_mask(w[1], h) | __hleu2_mask(w[2], h) | __hleu2_mask(w[3], h);
+      m = strict ? (__hltu2_mask(w[0], h) | __hltu2_mask(w[1], h) | __hltu2_mask(w[2], h) | __hltu2_mask(w[3], h))
+                 : (__hleu2_mask(w[0], h) | __hleu2_mask(w[1], h) | __hleu2_mask(w[2], h) | __hleu2_mask(w[3], h));
     return m != 0;
   }
 };
@@ -259,16 +285,18 @@ struct KeyTraits<KeyKind::BF16> {
   {
     return FloatRank<uint16_t, 16>::t_inv((uint16_t)(r ^ dirmask));
   }
-  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  __device__ __forceinline__ static bool may_pass(const uint4& v, Raw braw, Rank, bool is_max, bool strict)
   {
-    const __nv_bfloat16 e = __ushort_as_bfloat16(b.raw);
+    const __nv_bfloat16 e = __ushort_as_bfloat16(braw);
     const __nv_bfloat162 h = __halves2bfloat162(e, e);
     const __nv_bfloat162* w = reinterpret_cast<const __nv_bfloat162*>(&v);
     unsigned m;
     if (is_max)
-      m = __hgeu2_mask(w[0], h) | __hgeu2_mask(w[1], h) | __hgeu2_mask(w[2], h) | __hgeu2_mask(w[3], h);
+      m = strict ? (__hgtu2_mask(w[0], h) | __hgtu2_mask(w[1], h) | __hgtu2_mask(w[2], h) | __hgtu2_mask(w[3], h))
+                 : (__hgeu2_mask(w[0], h) | __hgeu2_mask(w[1], h) | __hgeu2_mask(w[2], h) | __hgeu2_mask(w[3], h));
     else
-      m = __hleu2_mask(w[0], h) | __hleu2_mask(w[1], h) | __hleu2_mask(w[2], h) | __hleu2_mask(w[3], h);
+      m = strict ? (__hltu2_mask(w[0], h) | __hltu2_mask(w[1], h) | __hltu2_mask(w[2], h) | __hltu2_mask(w[3], h))
+                 : (__hleu2_mask(w[0], h) | __hleu2_mask(w[1], h) | __hleu2_mask(w[2], h) | __hleu2_mask(w[3], h));
     return m != 0;
   }
 };
@@ -283,13 +311,18 @@ struct KeyTraits<KeyKind::F32> {
   {
     return FloatRank<uint32_t, 32>::t_inv(r ^ dirmask);
   }
-  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  __device__ __forceinline__ static bool may_pass(const uint4& v, Raw braw, Rank, bool is_max, bool strict)
   {
-    const float f = __uint_as_float(b.raw);
+    const float f = __uint_as_float(braw);
     const float x0 = __uint_as_float(v.x), x1 = __uint_as_float(v.y);
     const float x2 = __uint_as_float(v.z), x3 = __uint_as_float(v.w);
-    if (is_max)
+    if (is_max) {
+      if (strict)
+        return !(x0 <= f) | !(x1 <= f) | !(x2 <= f) | !(x3 <= f);
       return !(x0 < f) | !(x1 < f) | !(x2 < f) | !(x3 < f);
+    }
+    if (strict)
+      return !(x0 >= f) | !(x1 >= f) | !(x2 >= f) | !(x3 >= f);
     return !(x0 > f) | !(x1 > f) | !(x2 > f) | !(x3 > f);
   }
 };
@@ -312,11 +345,12 @@ struct KeyTraits<KeyKind::F64> {
     const int32_t x = (int32_t)hi;
     return x ^ (int32_t)((uint32_t)(x >> 31) >> 1);
   }
-  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  __device__ __forceinline__ static bool may_pass(const uint4& v, Raw braw, Rank, bool is_max, bool)
   {
-    // a key ranking below the bound is, as a number, at least (max) or at
-    // most (min) the bound key, so its high word compares likewise
-    const int32_t ob = order_hi((uint32_t)(b.raw >> 32));
+    // a key ranking at most the bound is, as a number, at least (max) or at
+    // most (min) the bound key, so its high word compares likewise (one
+    // compare of the high words cannot be strict, so this test never is)
+    const int32_t ob = order_hi((uint32_t)(braw >> 32));
     const int32_t o0 = order_hi(v.y), o1 = order_hi(v.w);
     if (is_max)
       return (o0 >= ob) | (o1 >= ob);
@@ -331,10 +365,12 @@ struct KeyTraits<KeyKind::U32> {
   static constexpr int kRankBits = 32;
   __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return x ^ dirmask; }
   __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask) { return r ^ dirmask; }
-  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  __device__ __forceinline__ static bool may_pass(const uint4& v, Raw, Rank brank, bool is_max, bool strict)
   {
     const uint32_t dm = is_max ? 0xffffffffu : 0u; // exact
-    return ((v.x ^ dm) < b.tau) | ((v.y ^ dm) < b.tau) | ((v.z ^ dm) < b.tau) | ((v.w ^ dm) < b.tau);
+    if (strict)
+      return ((v.x ^ dm) < brank) | ((v.y ^ dm) < brank) | ((v.z ^ dm) < brank) | ((v.w ^ dm) < brank);
+    return ((v.x ^ dm) <= brank) | ((v.y ^ dm) <= brank) | ((v.z ^ dm) <= brank) | ((v.w ^ dm) <= brank);
   }
 };
 
@@ -345,12 +381,66 @@ struct KeyTraits<KeyKind::I32> {
   static constexpr int kRankBits = 32;
   __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return (x ^ 0x80000000u) ^ dirmask; }
   __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask) { return (r ^ dirmask) ^ 0x80000000u; }
-  __device__ __forceinline__ static bool may_pass(const uint4& v, const Bound<Raw, Rank>& b, bool is_max)
+  __device__ __forceinline__ static bool may_pass(const uint4& v, Raw, Rank brank, bool is_max, bool strict)
   {
     const uint32_t dm = (is_max ? 0xffffffffu : 0u) ^ 0x80000000u; // exact
-    return ((v.x ^ dm) < b.tau) | ((v.y ^ dm) < b.tau) | ((v.z ^ dm) < b.tau) | ((v.w ^ dm) < b.tau);
+    if (strict)
+      return ((v.x ^ dm) < brank) | ((v.y ^ dm) < brank) | ((v.z ^ dm) < brank) | ((v.w ^ dm) < brank);
+    return ((v.x ^ dm) <= brank) | ((v.y ^ dm) <= brank) | ((v.z ^ dm) <= brank) | ((v.w ^ dm) <= brank);
   }
 };
+
+// ---------------------------------------------------------------------------
+// Keys of a 16-byte vector held in registers
+// ---------------------------------------------------------------------------
+// Key j of a 16-byte vector, and the vector with key j set (j is a
+// compile-time constant after unrolling; no local-memory views of registers).
+template <class Raw>
+__device__ __forceinline__ uint32_t vec_word(const uint4& v, int w)
+{
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+}
+template <class Raw>
+__device__ __forceinline__ Raw vec_key(const uint4& v, int j)
+{
+  if constexpr (sizeof(Raw) == 8)
+    return ((uint64_t)vec_word<Raw>(v, 2 * j + 1) << 32) | vec_word<Raw>(v, 2 * j);
+  else if constexpr (sizeof(Raw) == 4)
+    return vec_word<Raw>(v, j);
+  else
+    return (Raw)(vec_word<Raw>(v, j >> 1) >> (16 * (j & 1)));
+}
+__device__ __forceinline__ void vec_or_word(uint4& v, int w, uint32_t x)
+{
+  if (w == 0)
+    v.x |= x;
+  else if (w == 1)
+    v.y |= x;
+  else if (w == 2)
+    v.z |= x;
+  else
+    v.w |= x;
+}
+template <class Raw>
+__device__ __forceinline__ void vec_set_key(uint4& v, int j, Raw x) // slot j holds zero
+{
+  if constexpr (sizeof(Raw) == 8) {
+    vec_or_word(v, 2 * j, (uint32_t)x);
+    vec_or_word(v, 2 * j + 1, (uint32_t)((uint64_t)x >> 32));
+  } else if constexpr (sizeof(Raw) == 4) {
+    vec_or_word(v, j, (uint32_t)x);
+  } else {
+    vec_or_word(v, j >> 1, (uint32_t)x << (16 * (j & 1)));
+  }
+}
+
+// The value written for the element at segment-local index i: the payload,
+// or, with no payload array (an internal mode of the host-buffer entry
+// point), the index itself.
+__device__ __forceinline__ int32_t value_at(const int32_t* values, uint32_t i)
+{
+  return values ? values[i] : (int32_t)i;
+}
 
 // ---------------------------------------------------------------------------
 // Warp helpers

@@ -32,6 +32,9 @@ struct KeyOps {
   cudaError_t (*occupancy[kProfiles])(const LaunchShape& s, int* resident);
   // Read and clear this translation unit's device error word (synchronous).
   cudaError_t (*read_error)(uint32_t* word);
+  // Add this translation unit's statistics counters to out[0, 16) and clear
+  // them (synchronous; counted only by the statistics build).
+  cudaError_t (*read_stats)(unsigned long long* out);
 };
 
 const KeyOps& key_ops_f16();
@@ -43,5 +46,11 @@ const KeyOps& key_ops_i32();
 
 // Records a failed CUDA call for segtopk_last_cuda_error; returns SEGTOPK_ERROR_CUDA.
 int record_cuda_error(cudaError_t e);
+
+// Host-side check of a host offsets array (host-buffer entry points): every
+// offset non-negative and the addressed key count small enough for byte
+// arithmetic. Gives the number of keys addressed (the largest segment end)
+// and the longest segment. Returns a status code.
+int host_offsets_scan(const int64_t* offsets, int64_t num_segments, int64_t* num_keys, int64_t* max_len);
 
 } // namespace segtopk

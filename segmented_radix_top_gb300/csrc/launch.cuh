@@ -1,31 +1,52 @@
 // Launch helpers shared by the per-key-type translation units.
 #pragma once
 
+#include <mutex>
+
 #include "dispatch.h"
 #include "stream_topk.cuh"
 #include "warp_topk.cuh"
 
 namespace segtopk {
 
+// Per-device launch preparation of one kernel: the dynamic shared-memory
+// opt-in granted so far and the non-portable cluster permission. Function
+// attributes belong to each device's copy of a kernel, so they are tracked
+// per device ordinal, under a lock.
+struct DevicePrep {
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu;
+  uint32_t granted[kMaxDevices] = {};
+  bool nonportable[kMaxDevices] = {};
+  bool prepared[kMaxDevices] = {};
+};
+
 template <KeyKind KK, int NT, class PR>
 struct StreamLauncher {
   static cudaError_t prepare(uint32_t smem, int cluster)
   {
-    // Raise the dynamic shared-memory opt-in lazily, only as far as needed.
-    static uint32_t granted = 0;
-    static bool nonportable = false;
+    // Raise the dynamic shared-memory opt-in lazily, only as far as needed,
+    // on the current device.
+    static DevicePrep st;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+      return e;
+    if (dev < 0 || dev >= DevicePrep::kMaxDevices)
+      return cudaErrorInvalidDevice;
     auto fn = stream_topk_kernel<KK, NT, PR>;
-    if (smem > granted) {
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    std::lock_guard<std::mutex> lk(st.mu);
+    if (smem > st.granted[dev]) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess)
         return e;
-      granted = smem;
+      st.granted[dev] = smem;
     }
-    if (cluster > 8 && !nonportable) {
-      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (cluster > 8 && !st.nonportable[dev]) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess)
         return e;
-      nonportable = true;
+      st.nonportable[dev] = true;
     }
     return cudaSuccess;
   }
@@ -91,13 +112,22 @@ struct WarpLauncher {
     // Static shared memory only: ask for the largest shared-memory carveout,
     // so that the occupancy the launch bounds allow (32 one-warp CTAs, or four
     // eight-warp CTAs, per SM) is not cut by a small default carveout.
-    static bool prepared = false;
-    if (!prepared) {
-      cudaError_t e = cudaFuncSetAttribute(warp_topk_kernel<KK, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                           (int)cudaSharedmemCarveoutMaxShared);
-      if (e != cudaSuccess)
-        return e;
-      prepared = true;
+    static DevicePrep st;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+      return e;
+    if (dev < 0 || dev >= DevicePrep::kMaxDevices)
+      return cudaErrorInvalidDevice;
+    {
+      std::lock_guard<std::mutex> lk(st.mu);
+      if (!st.prepared[dev]) {
+        e = cudaFuncSetAttribute(warp_topk_kernel<KK, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+        if (e != cudaSuccess)
+          return e;
+        st.prepared[dev] = true;
+      }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.num_segments, 1, 1); // one segment per CTA
@@ -108,13 +138,28 @@ struct WarpLauncher {
   }
 };
 
-inline cudaError_t read_and_clear(uint32_t* word)
+// Both readers below have internal linkage: each translation unit reads its
+// own device words (an inline function would be merged across units).
+static inline cudaError_t read_and_clear(uint32_t* word)
 {
   uint32_t zero = 0;
   cudaError_t e = cudaMemcpyFromSymbol(word, g_device_error, sizeof(uint32_t));
   if (e != cudaSuccess)
     return e;
   return cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t));
+}
+
+// Adds this translation unit's statistics counters to out[0, kStatCount)
+// and clears them (synchronous).
+static inline cudaError_t read_and_clear_stats(unsigned long long* out)
+{
+  unsigned long long h[kStatCount] = {}, zero[kStatCount] = {};
+  cudaError_t e = cudaMemcpyFromSymbol(h, g_stats, sizeof(h));
+  if (e != cudaSuccess)
+    return e;
+  for (int i = 0; i < kStatCount; ++i)
+    out[i] += h[i];
+  return cudaMemcpyToSymbol(g_stats, zero, sizeof(zero));
 }
 
 } // namespace segtopk
@@ -130,7 +175,8 @@ inline cudaError_t read_and_clear(uint32_t* word)
                                {&WarpLauncher<KIND, 1>::launch, &WarpLauncher<KIND, kWarpTeam>::launch}, \
                                {&StreamLauncher<KIND, kCtaThreads, ProfileLong>::occupancy,        \
                                 &StreamLauncher<KIND, kCtaThreads, ProfileMany>::occupancy},       \
-                               &read_and_clear};                                                   \
+                               &read_and_clear,                                                    \
+                               &read_and_clear_stats};                                             \
     return ops;                                                                                    \
   }                                                                                                \
   }

@@ -25,8 +25,11 @@ std::mutex g_staging_mu;
 void* g_staging_addr[kMaxDevices]; // device address of g_noalloc_staging, per device (null: not set up)
 
 // The staging array's device address on the current device, looked up once
-// per device. The array's name in host code is only a handle the runtime
-// maps to the device copy; it is never passed to a kernel or a copy itself.
+// per device (with that device current) and kept for the life of the
+// process. The array's name in host code is only a handle the runtime maps
+// to the device copy; it is never passed to a kernel or a copy itself. A
+// device reset destroys the array's device copy, so the address is not
+// valid across one (the entry point's documentation says so).
 cudaError_t staging_address(void** out)
 {
   int dev = 0;
@@ -59,13 +62,15 @@ extern "C" int segtopk_batched_topk_host_noalloc(segtopk_dtype key_dtype, const 
 {
   using namespace segtopk;
   // Staging the request needs (the host-buffer path's workspace for these
-  // sizes); anything larger is refused before a byte is copied.
+  // sizes); anything larger is refused before a byte is copied. Offsets are
+  // checked first (non-negative), as the host-buffer path checks them.
   if (num_segments > 0 && k > 0 && segment_offsets) {
-    int64_t num_keys = 0;
-    for (int64_t s = 0; s < num_segments; ++s)
-      num_keys = segment_offsets[s + 1] > num_keys ? segment_offsets[s + 1] : num_keys;
+    int64_t num_keys = 0, max_len = 0;
+    const int v = host_offsets_scan(segment_offsets, num_segments, &num_keys, &max_len);
+    if (v != SEGTOPK_SUCCESS)
+      return v;
     const size_t need = segtopk_host_workspace_bytes(key_dtype, values != nullptr, num_keys, num_segments, k);
-    if (need > (size_t)SEGTOPK_NOALLOC_STAGING_BYTES)
+    if (need == 0 || need > (size_t)SEGTOPK_NOALLOC_STAGING_BYTES)
       return SEGTOPK_ERROR_NOT_SUPPORTED;
   }
   void* staging = nullptr;

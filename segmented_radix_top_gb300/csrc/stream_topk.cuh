@@ -76,7 +76,43 @@ struct KernelParams {
   float spec_z;          // its margin: mu + spec_z * sqrt(mu) + spec_c sample keys are kept
   float spec_c;
   int32_t spec_small;    // small targets by warp minimums (exact) rather than digit passes (slack stop)
+  long long wait_limit;  // clock cycles after which a wait on a bulk copy gives up
+  uint32_t test_extra_tx; // instrumented build only: bytes added to a slice's first copy's expected count
 };
+
+// Counters of the statistics build (per CTA, summed over the launch).
+enum StatIndex : int {
+  kStatCtas = 0,        // CTAs that served a segment slice
+  kStatCycles = 1,      // clock cycles from start to exit
+  kStatFirstBound = 2,  // cycles spent setting the first bound (sample or exact selection)
+  kStatStream = 3,      // cycles of the stream (first bound included)
+  kStatFinal = 4,       // cycles after the stream: final selection, merge, sort, output
+  kStatChunks = 5,      // ring chunks streamed
+  kStatTrims = 6,       // list trims during the stream
+  kStatRestreams = 7,   // slices read a second time (speculative bound too tight)
+  kStatListEntries = 8, // candidate-list entries at the end of the stream
+  kStatSpec = 9,        // slices whose first bound came from a sample
+  kStatDigitPasses = 10,// digit-selection passes (histogram passes) in the CTA
+  kStatWaitCycles = 11, // cycles thread 0 spent waiting for copies
+  kStatKeys = 12,       // keys of the slices
+  kStatSlowChunks = 13, // chunk shares of warp 0 that held candidates
+  kStatCount = 16
+};
+
+// Per-CTA counters of the statistics build, flushed once per CTA.
+static __device__ unsigned long long g_stats[kStatCount];
+
+#ifdef SEGTOPK_STATS
+#define SEGTOPK_STAT_ADD(i, v)                                                                     \
+  do {                                                                                             \
+    if (threadIdx.x == 0)                                                                          \
+      ctl.stat[(i)] += (unsigned long long)(v);                                                    \
+  } while (0)
+#else
+#define SEGTOPK_STAT_ADD(i, v)                                                                     \
+  do {                                                                                             \
+  } while (0)
+#endif
 
 // Host and device agree on the dynamic shared-memory layout.
 __host__ __device__ inline uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -130,6 +166,9 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
       raise_error(kErrSegmentTooLong);
     return;
   }
+#ifdef SEGTOPK_STATS
+  const long long t_start = clock64();
+#endif
   const uint32_t n = (uint32_t)n64;
   const uint32_t k = (uint32_t)p.k;
   const uint32_t m = k < n ? k : n;
@@ -148,6 +187,11 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   clear_slot<NT>(ctl.slot[2]);
   if (threadIdx.x == 0) {
     ctl.chunk_count[0] = ctl.chunk_count[1] = ctl.chunk_count[2] = 0;
+    ctl.abort = 0;
+#ifdef SEGTOPK_STATS
+    for (int i = 0; i < kStatCount; ++i)
+      ctl.stat[i] = 0;
+#endif
     ctl.gather_count = 0;
     ctl.front_base = 0;
     ctl.tie_base = 0;
@@ -158,8 +202,12 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   __syncthreads();
 
   // ---- this CTA's slice of the segment ----
+  // The body is the run of whole 16-byte vectors of the segment; the keys
+  // before its first vector (head) and after its last (tail) are read one by
+  // one. Any element-aligned key pointer works.
   const Raw* seg_keys = reinterpret_cast<const Raw*>(p.keys) + g0;
-  uint32_t head = (uint32_t)((VK - (int)(g0 % VK)) % VK); // unaligned leading keys
+  const uint32_t mis = (uint32_t)((reinterpret_cast<uintptr_t>(seg_keys) & 15u) / sizeof(Raw));
+  uint32_t head = (uint32_t)((VK - (int)mis) % VK); // unaligned leading keys
   if (head > n)
     head = n;
   const uint32_t body_v = (n - head) / VK;
@@ -170,6 +218,7 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   const uint32_t nchunks = (nvec + kChunkVec - 1) / kChunkVec;
   const bool has_head = rank == 0 && head > 0;
   const bool has_tail = rank == C - 1 && tail > 0;
+  SEGTOPK_STAT_ADD(kStatCtas, 1);
 
   auto chunk_of_step = [&](uint32_t s) { return fwd ? s : nchunks - 1 - s; };
   // ---- streaming selection state (uniform across the block) ----
@@ -208,7 +257,10 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     swap_lists();
     set_bound(kp.max_rank, kp.n);
   };
-  auto trim_list = [&](uint32_t slack) { select_union(nullptr, 0u, 0u, slack); };
+  auto trim_list = [&](uint32_t slack) {
+    SEGTOPK_STAT_ADD(kStatTrims, 1);
+    select_union(nullptr, 0u, 0u, slack);
+  };
 
   // Offer this thread's U vectors (vector j: vc[j] keys from slot 0, source
   // indices i0[j] + slot). Keys that may beat the bound are tested exactly;
@@ -219,7 +271,7 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     uint32_t mayv = 0;
 #pragma unroll
     for (int j = 0; j < U; ++j)
-      if (vc[j] && (open || TR::may_pass(vec[j], bound, is_max)))
+      if (vc[j] && (open || TR::may_pass(vec[j], bound.raw, bound.tau, is_max, true)))
         mayv |= 1u << j;
     bool overflow = false;
     if (mayv) {
@@ -287,10 +339,11 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const uint32_t t = (uint32_t)j * NT + threadIdx.x;
-      mayv |= (uint32_t)((t >= v0) & (t < v1) & TR::may_pass(vv[j], bound, is_max)) << j;
+      mayv |= (uint32_t)((t >= v0) & (t < v1) & TR::may_pass(vv[j], bound.raw, bound.tau, is_max, true)) << j;
     }
     if (!__any_sync(kFull, mayv != 0))
       return false; // the common case: nothing in this warp's share can enter the list
+    SEGTOPK_STAT_ADD(kStatSlowChunks, 1);
     const uint32_t lane = lane_id(), warp_base = threadIdx.x & ~31u;
     uint32_t cand[U], base[U], total = 0;
 #pragma unroll
@@ -399,21 +452,29 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   // speculative bound was used; the caller then checks that the slice gave
   // at least min(k, n_slice) entries.
   uint32_t gstep = 0; // ring steps over all passes (stage and mbarrier phase)
-  bool copies_ok = true;
   auto stream_pass = [&](bool allow_spec) {
+#ifdef SEGTOPK_STATS
+    const long long t_pass = clock64();
+#endif
     bool spec_used = false;
     const uint32_t gbase = gstep;
-    uint32_t issued = 0;
+    uint32_t issued = 0; // thread 0: chunks issued in this pass
+    uint32_t landed = 0; // thread 0: chunks 0 .. landed-1 seen complete
     auto issue_next = [&]() {
       const uint32_t g = gbase + issued;
       const uint32_t v0 = v_lo + chunk_of_step(issued) * kChunkVec;
       const uint32_t nv = min(kChunkVec, v_hi - v0);
       const uint32_t st = g % S;
-      mbar_arrive_expect_tx(&ctl.bars[st], nv * 16u);
+      uint32_t extra = 0;
+#ifdef SEGTOPK_TEST_HOOKS
+      if (issued == 0)
+        extra = p.test_extra_tx; // the wait on this copy then runs out (tests of the bounded wait)
+#endif
+      mbar_arrive_expect_tx(&ctl.bars[st], nv * 16u + extra);
       bulk_load(ring + (size_t)st * kChunkBytes, seg_keys + head + (size_t)v0 * VK, nv * 16u, &ctl.bars[st]);
       ++issued;
     };
-    if (threadIdx.x == 0 && copies_ok) {
+    if (threadIdx.x == 0 && !ctl.abort) {
       while (issued < S && issued < nchunks)
         issue_next();
     }
@@ -426,13 +487,25 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     for (uint32_t s = 0; s < nchunks; ++s) {
       const uint32_t g = gbase + s;
       const uint32_t st = g % S;
-      if (copies_ok)
-        copies_ok = mbar_wait(&ctl.bars[st], (g / S) & 1u);
+      // Every thread waits (bounded) for the stage. A wait that gives up
+      // sets the CTA's stop flag but changes no control flow: every thread
+      // still runs every barrier below, on whatever the stage holds, no
+      // further copy is issued, and the CTA writes no output.
+      if (!*reinterpret_cast<volatile uint32_t*>(&ctl.abort)) {
+#ifdef SEGTOPK_STATS
+        const long long tw = clock64();
+#endif
+        if (!mbar_wait(&ctl.bars[st], (g / S) & 1u, p.wait_limit))
+          atomicOr(&ctl.abort, 1u);
+        else if (threadIdx.x == 0)
+          landed = s + 1;
+        SEGTOPK_STAT_ADD(kStatWaitCycles, clock64() - tw);
+      }
       const uint32_t vb = v_lo + chunk_of_step(s) * kChunkVec;
       const uint32_t nv = min(kChunkVec, v_hi - vb);
       const uint4* stage = reinterpret_cast<const uint4*>(ring + (size_t)st * kChunkBytes);
       const Raw* stage_keys = reinterpret_cast<const Raw*>(stage);
-      const uint32_t nkeys = copies_ok ? nv * VK : 0u;
+      const uint32_t nkeys = nv * VK;
       const uint32_t idx0 = head + vb * VK;
       if (open) {
         if (count + nkeys <= k) {
@@ -444,6 +517,9 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
           __syncthreads();
           count += nkeys;
         } else {
+#ifdef SEGTOPK_STATS
+          const long long tb = clock64();
+#endif
           // the first bound, from the list and the most preferred keys of this
           // chunk (the rest of the chunk comes later in preference order and
           // is offered against it): speculative from p.spec_keys of them, else
@@ -504,46 +580,80 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
             if (!tied)
               select_union(stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nb * VK, trim_slack);
           }
+          SEGTOPK_STAT_ADD(kStatFirstBound, clock64() - tb);
           if (nb < nv)
             process_vectors(stage, fwd ? nb : 0u, fwd ? nv : nv - nb, idx0);
         }
-      } else if (copies_ok) {
+      } else {
         process_vectors(stage, 0u, nv, idx0);
       }
-      // every read of this stage is over: refill it
-      if (threadIdx.x == 0 && copies_ok && issued < nchunks)
+      // every read of this stage is over: refill it (only after this
+      // thread saw every copy so far land, and streaming goes on)
+      if (threadIdx.x == 0 && issued < nchunks && landed == s + 1 &&
+          !*reinterpret_cast<volatile uint32_t*>(&ctl.abort))
         issue_next();
     }
-    if (!copies_ok && threadIdx.x == 0) {
-      // let every copy still in flight land before this CTA's shared memory is released
-      for (uint32_t s = 0; s < issued; ++s)
-        mbar_wait(&ctl.bars[(gbase + s) % S], ((gbase + s) / S) & 1u);
+    if (threadIdx.x == 0) {
+      // after a wait gave up: let every copy still in flight land before
+      // this CTA's shared memory is released (each wait bounded)
+      for (uint32_t s = landed; s < issued; ++s)
+        mbar_wait(&ctl.bars[(gbase + s) % S], ((gbase + s) / S) & 1u, p.wait_limit);
     }
     gstep = gbase + nchunks;
+    SEGTOPK_STAT_ADD(kStatChunks, nchunks);
 
     if (has_tail && fwd)
       offer_edge(n - tail, tail);
     if (has_head && !fwd)
       offer_edge(0, head);
+    SEGTOPK_STAT_ADD(kStatStream, clock64() - t_pass);
+    __syncthreads(); // the stop flag is final for this pass
     return spec_used;
   };
 
-  if (stream_pass(true) && count < min(k, n_slice) && copies_ok) {
+  const bool spec_pass = stream_pass(true);
+  bool aborted = ctl.abort != 0;
+  if (!aborted && spec_pass && count < min(k, n_slice)) {
     // the sample misled the bound (an ordered slice): read the slice again
     // with bounds from exact selections only
+    SEGTOPK_STAT_ADD(kStatRestreams, 1);
     count = 0;
     open = true;
     bound = Bound<Raw, Rank>{(Rank)0, (Raw)0};
     __syncthreads();
     stream_pass(false);
+    aborted = ctl.abort != 0;
   }
+  SEGTOPK_STAT_ADD(kStatSpec, spec_pass ? 1 : 0);
+  SEGTOPK_STAT_ADD(kStatKeys, n_slice);
+  SEGTOPK_STAT_ADD(kStatListEntries, count);
+  if (aborted && C == 1)
+    return; // a wait gave up: no output (bit 0 of the device error word is set)
+#ifdef SEGTOPK_STATS
+  const long long t_final = clock64();
+  // flushes this CTA's counters once, at every exit below
+  auto flush_stats = [&]() {
+    SEGTOPK_STAT_ADD(kStatFinal, clock64() - t_final);
+    SEGTOPK_STAT_ADD(kStatCycles, clock64() - t_start);
+    SEGTOPK_STAT_ADD(kStatDigitPasses, sel_pass);
+    if (threadIdx.x == 0)
+      for (int i = 0; i < kStatCount; ++i)
+        if (ctl.stat[i])
+          atomicAdd(&g_stats[i], ctl.stat[i]);
+  };
+#define SEGTOPK_FLUSH_STATS() flush_stats()
+#else
+#define SEGTOPK_FLUSH_STATS()                                                                      \
+  do {                                                                                             \
+  } while (0)
+#endif
 
   // local top-k of this CTA's slice, for clusters that gather top-k lists
   // (a lone CTA selects once when writing the output; the histogram merge
   // works on whole lists: each holds its slice's top-k and, at the boundary
   // rank, a preference-order prefix of the slice's ties)
   __syncthreads();
-  if (count > k && C > 1 && p.merge_gather == 1)
+  if (count > k && C > 1 && p.merge_gather == 1 && !aborted)
     trim_list(0u);
 
   Raw* out_keys = reinterpret_cast<Raw*>(p.out_keys) + seg * (int64_t)k;
@@ -569,7 +679,7 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
       for (uint32_t e = threadIdx.x; e < mm; e += NT) {
         out_keys[e] = raw[e];
         if (out_values)
-          out_values[e] = values[idx[e]];
+          out_values[e] = value_at(values, idx[e]);
       }
     } else if (mm <= kCountMax) {
       finalize_small<TR, NT>(raw, idx, mm, mm, dirmask, pl, true, scratch, out_keys, out_values, values);
@@ -580,6 +690,7 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
 
   if (C == 1) {
     finish(list_raw, list_idx, count, spare_raw, spare_idx, ring);
+    SEGTOPK_FLUSH_STATS();
     return;
   }
 
@@ -601,6 +712,17 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     }
   }
   cluster_sync(); // every CTA has finished streaming and published its bound; every initialisation is visible
+  {
+    // a CTA whose copy wait gave up stops the whole cluster: every CTA reads
+    // every CTA's flag, and all leave after one more cluster barrier
+    uint32_t any = 0;
+    if (threadIdx.x < C)
+      any = dsmem_ld_u32(dsmem_map(smem_addr(&ctl.abort), threadIdx.x));
+    if (__syncthreads_or(any != 0)) {
+      cluster_sync();
+      return;
+    }
+  }
 
   if (p.merge_gather) {
     if (threadIdx.x < 32) {
@@ -655,10 +777,13 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
       }
     }
     cluster_sync(); // the leader holds every candidate
-    if (rank != leader)
+    if (rank != leader) {
+      SEGTOPK_FLUSH_STATS();
       return;
+    }
     unsigned char* scratch = ring + align16(cap * sizeof(Raw)) + align16(cap * 4u);
     finish(g_raw, g_idx, ctl.gather_count, list_raw, list_idx, scratch); // the leader's own lists are free now
+    SEGTOPK_FLUSH_STATS();
     return;
   }
 
@@ -766,8 +891,9 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
                         const uint32_t pos = position(cls, r1, r2);
                         out_keys[pos] = kr;
                         if (out_values)
-                          out_values[pos] = values[ki];
+                          out_values[pos] = value_at(values, ki);
                       });
+    SEGTOPK_FLUSH_STATS();
     return;
   }
 
@@ -784,9 +910,13 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
                       dsmem_st(gidx + pos * 4u, ki);
                     });
   cluster_sync(); // the leader holds all m items
-  if (rank != leader)
+  if (rank != leader) {
+    SEGTOPK_FLUSH_STATS();
     return;
+  }
   sort_and_write<TR, NT>(g_raw, g_idx, m, dirmask, scratch, out_keys, out_values, values);
+  SEGTOPK_FLUSH_STATS();
+#undef SEGTOPK_FLUSH_STATS
 }
 
 } // namespace segtopk

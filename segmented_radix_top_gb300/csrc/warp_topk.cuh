@@ -124,47 +124,6 @@ struct OutKey {
   }
 };
 
-// Key j of a 16-byte vector, and the vector with key j set (j is a
-// compile-time constant after unrolling; no local-memory views of registers).
-template <class Raw>
-__device__ __forceinline__ uint32_t vec_word(const uint4& v, int w)
-{
-  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
-}
-template <class Raw>
-__device__ __forceinline__ Raw vec_key(const uint4& v, int j)
-{
-  if constexpr (sizeof(Raw) == 8)
-    return ((uint64_t)vec_word<Raw>(v, 2 * j + 1) << 32) | vec_word<Raw>(v, 2 * j);
-  else if constexpr (sizeof(Raw) == 4)
-    return vec_word<Raw>(v, j);
-  else
-    return (Raw)(vec_word<Raw>(v, j >> 1) >> (16 * (j & 1)));
-}
-__device__ __forceinline__ void vec_or_word(uint4& v, int w, uint32_t x)
-{
-  if (w == 0)
-    v.x |= x;
-  else if (w == 1)
-    v.y |= x;
-  else if (w == 2)
-    v.z |= x;
-  else
-    v.w |= x;
-}
-template <class Raw>
-__device__ __forceinline__ void vec_set_key(uint4& v, int j, Raw x) // slot j holds zero
-{
-  if constexpr (sizeof(Raw) == 8) {
-    vec_or_word(v, 2 * j, (uint32_t)x);
-    vec_or_word(v, 2 * j + 1, (uint32_t)((uint64_t)x >> 32));
-  } else if constexpr (sizeof(Raw) == 4) {
-    vec_or_word(v, j, (uint32_t)x);
-  } else {
-    vec_or_word(v, j >> 1, (uint32_t)x << (16 * (j & 1)));
-  }
-}
-
 // One segment per CTA of W warps (W = 1 for short segments, 8 for longer
 // ones), k <= 32, serving segments with n_lo < n <= n_hi. Warp w reads rounds
 // w, w + W, ... of 32 * U 16-byte vectors and keeps its own top list. Its
@@ -214,7 +173,12 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
   const bool is_max = dirmask != 0;
   const bool pl = p.prefer_larger != 0;
   const Raw* keys = reinterpret_cast<const Raw*>(p.keys);
-  const uint4* kvec = reinterpret_cast<const uint4*>(p.keys); // the key array is 16-byte aligned
+  // 16-byte vectors are taken from the aligned address at or below keys[0];
+  // in that vector array, key i of the key array is element i + lead
+  const uintptr_t kaddr = reinterpret_cast<uintptr_t>(p.keys);
+  const uint4* kvec = reinterpret_cast<const uint4*>(kaddr & ~(uintptr_t)15);
+  const int64_t lead = (int64_t)((kaddr & 15u) / sizeof(Raw));
+  const int64_t a0 = g0 + lead, a1 = g1 + lead; // the segment in vector-array elements
   if (W > 1) {
     if (threadIdx.x == 0)
       shared_bound = ~0ull;
@@ -227,9 +191,10 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
   uint64_t shb = ~0ull; // this warp's copy of shared_bound (W > 1)
   uint32_t qn = 0;      // queued candidates (warp-uniform)
   // Raw-domain prefilter of whole vectors: a key can enter only if its rank
-  // is at most the bound's rank (open: no such bound yet).
+  // is at most the bound's rank brank (bits braw; open: no such bound yet).
   bool open = true;
-  Bound<Raw, Rank> bound{(Rank)0, (Raw)0};
+  Rank brank = 0;
+  Raw braw = 0;
 
   // does composite c beat the k-th entry (and the shared bound)?
   auto beats = [&](const E& c) {
@@ -245,8 +210,10 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
       tr = sr < tr ? sr : tr;
     }
     open = tr >= kMaxRank; // an empty slot, or a rank that admits every key
-    if (!open)
-      bound = Bound<Raw, Rank>{(Rank)(tr + 1), TR::unrank(tr, dirmask)};
+    if (!open) {
+      brank = tr;
+      braw = TR::unrank(tr, dirmask);
+    }
   };
   auto refresh_shared = [&]() { // warp-uniform read of the shared bound
     if (W > 1) {
@@ -275,10 +242,11 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
   auto composite = [&](Raw key, uint32_t idx) { return E::make(TR::rank(key, dirmask), pl ? ~idx : idx); };
 
   // 16-byte vectors covering the segment. A vector is read whole when it ends
-  // inside the segment (its start is at or after the array's aligned start);
-  // the last, partial one key by key.
-  const int64_t v_first = g0 / VK;
-  const int64_t v_end = (g1 + VK - 1) / VK;
+  // inside the segment (its start, if before the segment, is still inside
+  // the aligned 16 bytes that hold the segment's first key); the last,
+  // partial one key by key.
+  const int64_t v_first = a0 / VK;
+  const int64_t v_end = (a1 + VK - 1) / VK;
   bool first = true;
   for (int64_t vb = v_first + (int64_t)warp * 32 * U; vb < v_end; vb += (int64_t)32 * U * W) {
     uint4 vec[U];
@@ -287,12 +255,12 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
       const int64_t v = vb + u * 32 + lane;
       vec[u] = make_uint4(0, 0, 0, 0);
       if (v < v_end) {
-        if ((v + 1) * VK <= g1) {
+        if ((v + 1) * VK <= a1) {
           vec[u] = __ldg(kvec + v);
         } else {
 #pragma unroll
           for (int j = 0; j < VK; ++j) {
-            const int64_t e = v * VK + j;
+            const int64_t e = v * VK + j - lead; // key-array index
             if (e >= g0 && e < g1)
               vec_set_key<Raw>(vec[u], j, keys[e]);
           }
@@ -306,7 +274,7 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
       int best_s = -1;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t rel = (vb + u * 32 + lane) * VK - g0;
+        const int64_t rel = (vb + u * 32 + lane) * VK - a0;
 #pragma unroll
         for (int j = 0; j < VK; ++j) {
           if (rel + j >= 0 && rel + j < (int64_t)n) {
@@ -336,12 +304,12 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t v = vb + u * 32 + lane;
-      const int64_t rel = v * VK - g0; // segment index of key 0 of the vector
+      const int64_t rel = v * VK - a0; // segment index of key 0 of the vector
       const int lo = rel < 0 ? (int)-rel : 0;
       const int64_t rest = (int64_t)n - rel; // keys of the segment from key 0 of the vector on
       const int hi = rest < VK ? (int)rest : VK;
       stage[u][lane] = vec[u];
-      if (hi > lo && (open || TR::may_pass(vec[u], bound, is_max))) {
+      if (hi > lo && (open || TR::may_pass(vec[u], braw, brank, is_max, false))) {
 #pragma unroll
         for (int j = 0; j < VK; ++j) {
           if (j >= lo && j < hi && beats(composite(vec_key<Raw>(vec[u], j), (uint32_t)(rel + j))))
@@ -360,7 +328,7 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
         cand &= cand - 1;
         const int u = s / VK, j = s % VK;
         const Raw key = reinterpret_cast<const Raw*>(&stage[u][lane])[j];
-        c = composite(key, (uint32_t)((vb + u * 32 + lane) * VK + j - g0));
+        c = composite(key, (uint32_t)((vb + u * 32 + lane) * VK + j - a0));
         enter = beats(c);
       }
       uint32_t mask = __ballot_sync(kFull, enter);
@@ -406,7 +374,7 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
     Raw* out_keys = reinterpret_cast<Raw*>(p.out_keys) + seg * (int64_t)k;
     out_keys[lane] = keys[g0 + idx];
     if (p.out_values)
-      p.out_values[seg * (int64_t)k + lane] = p.values[g0 + idx];
+      p.out_values[seg * (int64_t)k + lane] = p.values ? p.values[g0 + idx] : (int32_t)idx;
   }
 }
 

@@ -27,7 +27,7 @@ def to_device_keys(wl: W.Workload, device="cuda") -> torch.Tensor:
 
 def run_gpu(wl: W.Workload, cluster_width: int = 0, max_segment_len="auto", device="cuda",
             values: np.ndarray | None = "workload", keys_t=None, stream=None, small_segment_max_len: int = 0,
-            team_segment_max_len: int = 0):
+            team_segment_max_len: int = 0, lib=None):
     """Returns (out_key_bits [S*k] storage dtype, out_values or None) as numpy."""
     if keys_t is None:
         keys_t = to_device_keys(wl, device)
@@ -46,7 +46,7 @@ def run_gpu(wl: W.Workload, cluster_width: int = 0, max_segment_len="auto", devi
                     determinism=wl.determinism, tie_break=wl.tie_break, ordering=wl.ordering,
                     out_keys=out_k, out_values=out_v, max_segment_len=ml,
                     cluster_width=cluster_width, stream=stream, small_segment_max_len=small_segment_max_len,
-                    team_segment_max_len=team_segment_max_len)
+                    team_segment_max_len=team_segment_max_len, lib=lib)
     torch.cuda.synchronize()
     gk = out_k.cpu().numpy().view(W.STORAGE[wl.dtype] if wl.dtype != "i32" else np.uint32)
     if wl.dtype == "i32":
@@ -123,6 +123,6 @@ def check_workload(wl: W.Workload, cluster_width: int = 0, where: str = "", **kw
     got_k, got_v = run_gpu(wl, cluster_width=cluster_width, **kw)
     want_k, want_v = run_oracle(wl, values=kw.get("values", "workload"))
     compare(wl, got_k, got_v, want_k, want_v, where=where or wl.name)
-    err = st.read_device_error()
+    err = st.read_device_error(lib=kw.get("lib"))
     assert err == 0, "device error word %#x" % err
     return got_k, got_v

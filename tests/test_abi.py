@@ -65,9 +65,27 @@ def test_noop_and_sizes(lib):
     assert call(lib, out_keys=0) == 1
     assert call(lib, values=256) == 1            # values without out_values
     assert call(lib, out_values=256) == 1        # out_values without values
-    assert call(lib, keys=18) == 4               # misaligned keys
+    assert call(lib, keys=18) == 4               # keys not aligned to the element size (f32)
+    assert call(lib, dtype=0, keys=17) == 4      # f16 keys at an odd address
+    assert call(lib, dtype=3, keys=20) == 4      # f64 keys 4-byte aligned only
     assert call(lib, k=B.MAX_K + 1) == 3
     assert call(lib, max_len=(1 << 31)) == 3
+
+
+def test_element_aligned_keys_pass_validation(lib):
+    # keys need only element alignment: an offset view of a larger array is
+    # accepted (without a device the call then fails at the device query)
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake pointers must not reach a launch on a machine with a GPU")
+    assert call(lib, keys=20) == 5               # f32 at 4-byte alignment: validated, then no device
+    assert call(lib, dtype=0, keys=18) == 5      # f16 at 2-byte alignment
+
+
+def test_diagnostics_are_off_in_the_ordinary_build(lib):
+    arr = (ctypes.c_uint64 * 16)()
+    assert lib.segtopk_read_stats(arr, 16) == 3
+    assert lib.segtopk_set_test_hooks(1000, 16) == 3
 
 
 def test_status_strings(lib):
@@ -91,10 +109,53 @@ def test_options_validation(lib):
 
 
 def test_workspace_bytes(lib):
+    # keys, offsets and output keys; pairs add the selected source indices
+    # (values stay on the host)
     a = st.host_workspace_bytes("f32", False, 1000, 10, 8)
     b = st.host_workspace_bytes("f32", True, 1000, 10, 8)
-    assert a >= 4000 + 88 + 320 and b >= a + 4000 + 320
+    assert a >= 4000 + 88 + 320 and b >= a + 320
+    assert b < a + 4000  # no device copy of the values
     assert st.host_workspace_bytes("f32", True, -1, 10, 8) == 0
+    assert st.host_workspace_bytes("f64", False, 1 << 62, 1, 8) == 0  # byte count would overflow
+
+
+def _host_call(lib, offsets, values=False, noalloc=False, k=4):
+    """Host-buffer entry points with real host arrays and a fake (never
+    touched) device workspace: the checks below fail before any copy."""
+    import numpy as np
+    offs = np.ascontiguousarray(offsets, dtype=np.int64)
+    n = max(int(offs.max()), 1)
+    keys = np.zeros(n, dtype=np.float32)
+    vals = np.zeros(n, dtype=np.int32) if values else None
+    nseg = len(offs) - 1
+    ok = np.zeros(nseg * k, dtype=np.float32)
+    ov = np.zeros(nseg * k, dtype=np.int32) if values else None
+    vp = ctypes.c_void_p
+    args = [2, vp(keys.ctypes.data), vp(vals.ctypes.data) if values else None, vp(offs.ctypes.data), nseg, k,
+            0, 2, 1, 2, vp(ok.ctypes.data), vp(ov.ctypes.data) if values else None, -1]
+    if noalloc:
+        return lib.segtopk_batched_topk_host_noalloc(*args, None)
+    return lib.segtopk_batched_topk_host(*args, vp(256), 1 << 30, None)
+
+
+def test_host_path_rejects_negative_offsets(lib):
+    # a negative offset would make the kernel read before the key array
+    for noalloc in (False, True):
+        for offs in ([-4, 10], [0, 5, -1, 8], [-1, -1]):
+            for values in (False, True):
+                assert _host_call(lib, offs, values=values, noalloc=noalloc) == 1
+                assert lib.segtopk_last_launch_count() == 0
+
+
+def test_host_path_rejects_unaligned_workspace(lib):
+    import numpy as np
+    keys = np.zeros(8, dtype=np.float32)
+    offs = np.array([0, 8], dtype=np.int64)
+    ok = np.zeros(4, dtype=np.float32)
+    vp = ctypes.c_void_p
+    rc = lib.segtopk_batched_topk_host(2, vp(keys.ctypes.data), None, vp(offs.ctypes.data), 1, 4, 0, 2, 1, 2,
+                                       vp(ok.ctypes.data), None, -1, vp(256 + 16), 1 << 20, None)
+    assert rc == 4
 
 
 def _header_text():

@@ -164,3 +164,54 @@ def test_many_single_cta_segments(dtype):
         wl = W.random_workload(900 + i, dtype, lengths, k, direction, "gpu_to_gpu", tie, ordering,
                                pairs=(i % 2 == 0), distinct=(40 if i == 1 else None), lead=1 + i)
         check_workload(wl, cluster_width=1, where="many segments %s k=%d %s %s" % (dtype, k, tie, ordering))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "f32", "f64", "u32"])
+def test_offset_view_of_the_key_array(dtype):
+    """keys[1:] of a device array: the key pointer is aligned to its element
+    size only, so no segment starts on a 16-byte boundary of the pointer's
+    own array; every path (single warp, team, CTA, cluster) reads it."""
+    from tests.gpu_util import to_device_keys
+    lengths = [0, 1, 5, 31, 33, 700, 4095, 9000, 40001, 150000]
+    for i, (k, width, small, team) in enumerate([(8, 0, 0, 0), (32, 1, -1, -1), (300, 0, 0, 0),
+                                                 (50, 3, -1, -1), (16, 0, 100000, -1), (24, 0, -1, 100000)]):
+        full = W.random_workload(900 + i, dtype, lengths, k, "max" if i % 2 else "min", "gpu_to_gpu",
+                                 ["prefer_smaller_index", "prefer_larger_index"][i % 2],
+                                 ["stable_sorted", "unsorted"][i % 2], pairs=True, distinct=200, lead=1)
+        wl = W.Workload("view", dtype, full.keys[1:], full.values[1:], full.offsets - 1, k, full.direction,
+                        full.determinism, full.tie_break, full.ordering)
+        keys_full = to_device_keys(full)
+        view = keys_full[1:]
+        assert view.data_ptr() % 16 != 0
+        check_workload(wl, cluster_width=width, keys_t=view, small_segment_max_len=small,
+                       team_segment_max_len=team, where="%s view k=%d C=%d" % (dtype, k, width))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32", "f64", "u32", "i32"])
+def test_too_small_length_hint_is_reported(dtype):
+    """A max_segment_len hint below the longest segment is a caller error:
+    the longer segments are left unwritten and bit 1 of the device error word
+    is set, read back per key type (every kernel translation unit has its
+    own word); the other segments are still exact."""
+    import segmented_radix_top_gb300 as st
+    from tests.gpu_util import SENTINEL_VALUE, compare, run_oracle
+    lengths = [10, 3000, 9000, 60000, 100]
+    for k, width in [(8, 0), (50, 1), (50, 2)]:
+        wl = W.random_workload(950 + k + width, dtype, lengths, k, "max", "gpu_to_gpu", "prefer_smaller_index",
+                               "stable_sorted", pairs=True, distinct=100, lead=1)
+        assert st.read_device_error() == 0
+        got_k, got_v = run_gpu(wl, cluster_width=width, max_segment_len=9000)
+        err = st.read_device_error()
+        assert err == 2, "error word %#x (want the segment-too-long bit)" % err
+        v = got_v.reshape(wl.num_segments, k)
+        assert np.all(v[3] == SENTINEL_VALUE)  # the 60000-key segment is left unwritten
+        keep = np.array([0, 1, 2, 4])
+        sub = W.Workload("hint", dtype, wl.keys, wl.values, wl.offsets, k, wl.direction, wl.determinism,
+                         wl.tie_break, wl.ordering)
+        want_k, want_v = run_oracle(sub)
+        gk, wk = got_k.reshape(-1, k)[keep].reshape(-1), want_k.reshape(-1, k)[keep].reshape(-1)
+        gv, wv = v[keep].reshape(-1), want_v.reshape(-1, k)[keep].reshape(-1)
+        offs = np.concatenate([[0], np.cumsum(np.array(lengths)[keep])])
+        part = W.Workload("hint", dtype, np.zeros(int(offs[-1]), dtype=wl.keys.dtype), None, offs, k,
+                          wl.direction, wl.determinism, wl.tie_break, wl.ordering)
+        compare(part, gk, gv, wk, wv, where="%s k=%d C=%d short segments" % (dtype, k, width))

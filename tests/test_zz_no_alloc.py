@@ -98,3 +98,31 @@ def test_request_beyond_the_staging_size_is_refused():
     with pytest.raises(st.SegTopKError) as e:
         st.batched_topk_host_noalloc("f32", keys, offs, 4)
     assert e.value.name == "NOT_SUPPORTED"
+
+
+def test_calls_allocate_no_device_memory():
+    # the property the entry point exists for: after a first call of each
+    # shape (which loads the kernels and looks up the staging address), more
+    # calls of those shapes leave the device's free memory and torch's
+    # allocator untouched
+    shapes = [W.random_workload(7100, "f32", [3, 900, 20000], 50, pairs=True, distinct=100, lead=1),
+              W.random_workload(7101, "f16", [1, 5000, 70000], 16, "min", pairs=False),
+              W.workload1()]
+
+    def call(wl):
+        keys, offs, vals, out_k, out_v = host_tensors(wl)
+        st.batched_topk_host_noalloc(wl.dtype, keys, offs, wl.k, values=vals, direction=wl.direction,
+                                     determinism=wl.determinism, tie_break=wl.tie_break, ordering=wl.ordering,
+                                     out_keys=out_k, out_values=out_v, max_segment_len=wl.max_segment_len)
+
+    for wl in shapes:
+        call(wl)
+    torch.cuda.synchronize()
+    free0, allocated0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    for _ in range(3):
+        for wl in shapes:
+            call(wl)
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free0, "device free memory changed across no-allocation calls"
+    assert torch.cuda.memory_allocated() == allocated0
+    assert st.read_device_error() == 0
