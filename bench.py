@@ -58,6 +58,8 @@ def workload_for(name: str):
         return W.workload5(mode="det")
     if name == "5":
         return W.workload5(mode="nondet")
+    if name == "array":
+        return W.array_workload()
     return W.by_number(int(name))
 
 
@@ -66,6 +68,8 @@ def kernel_label(wl, launches: int, sms: int) -> str:
     warp-select kernel (one warp each with many segments, eight with few),
     longer ones the CTA / cluster kernel."""
     cta = "stream_topk_kernel<%s>" % wl.dtype
+    if wl.info.get("array"):
+        return "fill_piece_offsets + %s (pass 1, pieces) + %s (pass 2, candidates)" % (cta, cta)
     if wl.k > 32:
         return cta
     few = wl.num_segments < sms
@@ -322,7 +326,7 @@ NUMPY_SIGNED = {"f16": np.int16, "bf16": np.int16, "f32": np.int32, "f64": np.in
                 "i32": np.int32}
 # every workload of a default run (5: not_guaranteed + unsorted, 5det: gpu_to_gpu + stable_sorted);
 # the headline is the largest configuration in its deterministic mode
-ALL_WORKLOADS = ["1", "2", "3", "4", "5", "5det"]
+ALL_WORKLOADS = ["1", "2", "3", "4", "5", "5det", "array"]
 HEADLINE = "5det"
 
 
@@ -344,10 +348,22 @@ class Resident:
         self.out_k = torch.empty(wl.num_segments * wl.k, dtype=tv, device=dev)
         self.out_v = torch.empty(wl.num_segments * wl.k, dtype=torch.int32, device=dev) \
             if wl.values is not None else None
+        self.array = bool(wl.info.get("array"))
+        if self.array:
+            import segmented_radix_top_gb300 as st
+            need = st.load().segtopk_topk_workspace_bytes(st.DTYPE[wl.dtype], 4 if wl.values is not None else 0,
+                                                          wl.num_keys, wl.k)
+            self.workspace = torch.empty(max(int(need), 256), dtype=torch.uint8, device=dev)
 
     def call(self, i, lib=None):
         import segmented_radix_top_gb300 as st
         wl = self.wl
+        if self.array:
+            st.topk(self.keys[i % self.copies], wl.k, values=self.vals[i % self.copies] if self.vals else None,
+                    key_dtype=wl.dtype, direction=wl.direction, determinism=wl.determinism,
+                    tie_break=wl.tie_break, ordering=wl.ordering, out_keys=self.out_k, out_values=self.out_v,
+                    workspace=self.workspace, lib=lib)
+            return
         st.batched_topk(self.keys[i % self.copies], self.offs, wl.k,
                         values=self.vals[i % self.copies] if self.vals else None, key_dtype=wl.dtype,
                         direction=wl.direction, determinism=wl.determinism, tie_break=wl.tie_break,
@@ -502,10 +518,13 @@ def run_ours(args, ws, rank, local):
                            props.multi_processor_count, ws, args.steps)
         del res
         torch.cuda.empty_cache()
-        e2e_steps = max(1, min(args.steps, 10 if name == headline else 3))
-        e2e_v, h2d, d2h, e2e_n = time_e2e(wl, e2e_steps, dev, ws)
-        line["e2e"] = {"value": e2e_v, "unit": "keys/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                       "steps": e2e_n}
+        if wl.info.get("array"):
+            line["e2e"] = None  # the single-array entry point takes device buffers only
+        else:
+            e2e_steps = max(1, min(args.steps, 10 if name == headline else 3))
+            e2e_v, h2d, d2h, e2e_n = time_e2e(wl, e2e_steps, dev, ws)
+            line["e2e"] = {"value": e2e_v, "unit": "keys/s", "h2d_bytes_per_step": h2d,
+                           "d2h_bytes_per_step": d2h, "steps": e2e_n}
         torch.cuda.empty_cache()
         per[name] = line
         if name == headline:

@@ -56,8 +56,10 @@ typedef enum {
 } segtopk_determinism;
 
 /* Boundary tie policy (same page, "Tie-break" table). A concrete tie-break
- * requires SEGTOPK_GPU_TO_GPU; UNSPECIFIED is resolved as
- * PREFER_SMALLER_INDEX by this library in every determinism mode. */
+ * requires SEGTOPK_GPU_TO_GPU. UNSPECIFIED is resolved as
+ * PREFER_SMALLER_INDEX under RUN_TO_RUN and GPU_TO_GPU; under
+ * NOT_GUARANTEED, boundary ties beyond those needed are taken in whatever
+ * order the kernel meets them (any subset of the ties is a valid result). */
 typedef enum {
   SEGTOPK_TIE_UNSPECIFIED = 0,
   SEGTOPK_PREFER_SMALLER_INDEX = 1,
@@ -69,7 +71,9 @@ typedef enum {
  *         positions may differ from run to run (set membership, not
  *         positions, is what determinism pins).
  * SORTED: by key, better first; equal keys in unspecified order (this
- *         library writes them in source-index order, i.e. as STABLE_SORTED).
+ *         library sorts 64-bit keys on the key alone; single-warp paths
+ *         with larger indices preferred write equal keys by descending
+ *         index; otherwise equal keys come out in source-index order).
  * STABLE_SORTED: by key, better first; equal keys by source index ascending,
  *         whatever the tie-break. */
 typedef enum {
@@ -188,6 +192,60 @@ SEGTOPK_API int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* key
                             segtopk_tie_break tie_break, segtopk_ordering ordering, void* out_keys,
                             int32_t* out_values, int64_t max_segment_len,
                             const segtopk_options* options, void* stream);
+
+/*
+ * segtopk_batched_topk_ex with a payload of 4- or 8-byte values: values and
+ * out_values point to value_bytes-wide elements (int32_t or int64_t; any
+ * 8-byte payload, such as a global index or a pointer, is copied as is).
+ * value_bytes must be 4 or 8 when values is not NULL (else
+ * SEGTOPK_ERROR_INVALID_VALUE). Everything else is as in
+ * segtopk_batched_topk_ex; keys only when values and out_values are NULL.
+ * (The pages' CUB pull request lists wider value types and larger segments
+ * among its future work: "Implement Segmented TopK using
+ * Thread-Block-Clusters", section 10 "Known limitations and future work".)
+ */
+SEGTOPK_API int segtopk_batched_topk_values(segtopk_dtype key_dtype, const void* keys, const void* values,
+                                            int32_t value_bytes, const int64_t* segment_offsets,
+                                            int64_t num_segments, int32_t k, segtopk_direction direction,
+                                            segtopk_determinism determinism, segtopk_tie_break tie_break,
+                                            segtopk_ordering ordering, void* out_keys, void* out_values,
+                                            int64_t max_segment_len, const segtopk_options* options,
+                                            void* stream);
+
+/*
+ * Top-k over one array (no segments): the k best of keys[0, num_keys),
+ * with the same contract per mode as one segment of segtopk_batched_topk
+ * (source index = array index). The CUB pull request's overview names this
+ * operation (cub::DeviceTopK) beside the segmented one ("Implement Segmented
+ * TopK using Thread-Block-Clusters", section 1.1).
+ *
+ * Method: two passes of the segmented selection. The array is split into P
+ * balanced contiguous pieces (P = min(304, num_keys / max(65536, 16 k)), at
+ * least 1); pass 1 writes each piece's k best, in stable sorted order, to the
+ * workspace; pass 2 selects the k best of the P * k candidates. Pieces keep
+ * source order and each piece's equal keys keep index order, so a
+ * candidate's position orders ties as its array index does: tie-breaks and
+ * stable order are exact.
+ *
+ * Arguments: keys, values, out_keys, out_values, workspace are device
+ * pointers. values / out_values: optional payload of value_bytes (4 or 8)
+ * per element, both NULL for keys only. out_keys / out_values hold k slots;
+ * with num_keys < k only the first num_keys are written. workspace: at
+ * least segtopk_topk_workspace_bytes(...) bytes, 256-byte aligned, owned by
+ * the caller (the library allocates nothing). num_keys may exceed 2^31 as
+ * long as every piece holds fewer than 2^31 keys.
+ *
+ * Errors as segtopk_batched_topk; a workspace that is too small returns
+ * SEGTOPK_ERROR_INVALID_VALUE. Asynchronous on `stream` (up to three kernel
+ * launches: the piece offsets, pass 1, pass 2).
+ */
+SEGTOPK_API size_t segtopk_topk_workspace_bytes(segtopk_dtype key_dtype, int32_t value_bytes, int64_t num_keys,
+                                                int32_t k);
+SEGTOPK_API int segtopk_topk(segtopk_dtype key_dtype, const void* keys, const void* values, int32_t value_bytes,
+                             int64_t num_keys, int32_t k, segtopk_direction direction,
+                             segtopk_determinism determinism, segtopk_tie_break tie_break,
+                             segtopk_ordering ordering, void* out_keys, void* out_values, void* workspace,
+                             size_t workspace_bytes, void* stream);
 
 /*
  * Same operation with HOST buffers: keys, values, segment_offsets, out_keys

@@ -9,7 +9,7 @@ from ._binding import (DETERMINISM, DIRECTION, DTYPE, KEY_BYTES, MAX_K, NOALLOC_
                        ORDERING, TIE_BREAK, SegTopKError, batched_topk, batched_topk_host,
                        batched_topk_host_noalloc, host_workspace_bytes,
                        last_launch_count, library_path, load, load_instrumented, read_device_error,
-                       read_stats, set_test_hooks)
+                       read_stats, set_test_hooks, topk)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:

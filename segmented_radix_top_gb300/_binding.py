@@ -84,6 +84,14 @@ def _open(path):
     L.segtopk_batched_topk_ex.restype = c_int
     L.segtopk_batched_topk_ex.argtypes = [c_int, vp, vp, vp, c_i64, c_i32, c_int, c_int, c_int, c_int,
                                           vp, vp, c_i64, ctypes.POINTER(Options), vp]
+    L.segtopk_batched_topk_values.restype = c_int
+    L.segtopk_batched_topk_values.argtypes = [c_int, vp, vp, c_i32, vp, c_i64, c_i32, c_int, c_int, c_int, c_int,
+                                              vp, vp, c_i64, ctypes.POINTER(Options), vp]
+    L.segtopk_topk.restype = c_int
+    L.segtopk_topk.argtypes = [c_int, vp, vp, c_i32, c_i64, c_i32, c_int, c_int, c_int, c_int, vp, vp, vp,
+                               ctypes.c_size_t, vp]
+    L.segtopk_topk_workspace_bytes.restype = ctypes.c_size_t
+    L.segtopk_topk_workspace_bytes.argtypes = [c_int, c_i32, c_i64, c_i32]
     L.segtopk_batched_topk_host.restype = c_int
     L.segtopk_batched_topk_host.argtypes = [c_int, vp, vp, vp, c_i64, c_i32, c_int, c_int, c_int,
                                             c_int, vp, vp, c_i64, vp, ctypes.c_size_t, vp]
@@ -148,6 +156,8 @@ def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, v
     size); its element size must match the key type (a raw-bits tensor of
     the same width works with key_dtype).
     segment_offsets: int64 CUDA tensor of num_segments + 1 offsets.
+    values: optional int32 or int64 CUDA tensor parallel to keys (int64
+    values take segtopk_batched_topk_values).
     Returns (out_keys, out_values) of shape [num_segments * k]; out_values is
     None for keys-only calls. Slots past a short segment's length are left as
     they were in the given out tensors (uninitialised if allocated here).
@@ -164,18 +174,59 @@ def batched_topk(keys: torch.Tensor, segment_offsets: torch.Tensor, k: int, *, v
     num_segments = segment_offsets.numel() - 1
     if out_keys is None:
         out_keys = torch.empty(max(num_segments, 0) * k, dtype=keys.dtype, device=keys.device)
+    wide = values is not None and values.dtype == torch.int64
+    if values is not None and values.dtype not in (torch.int32, torch.int64):
+        raise ValueError("values must be int32 or int64")
     if values is not None and out_values is None:
-        out_values = torch.empty(max(num_segments, 0) * k, dtype=torch.int32, device=keys.device)
+        out_values = torch.empty(max(num_segments, 0) * k, dtype=values.dtype, device=keys.device)
+    if values is not None and out_values.dtype != values.dtype:
+        raise ValueError("out_values must have the dtype of values")
     ml = -1 if max_segment_len is None else int(max_segment_len)
     opts = Options()
     opts.cluster_width = int(cluster_width)
     opts.small_segment_max_len = int(small_segment_max_len)
     opts.team_segment_max_len = int(team_segment_max_len)
-    rc = L.segtopk_batched_topk_ex(DTYPE[kd], _ptr(keys), _ptr(values), _ptr(segment_offsets),
-                                   num_segments, int(k), DIRECTION[direction],
-                                   DETERMINISM[determinism], TIE_BREAK[tie_break], ORDERING[ordering],
-                                   _ptr(out_keys), _ptr(out_values), ml, ctypes.byref(opts),
-                                   _stream_handle(stream, keys.device))
+    if wide:
+        rc = L.segtopk_batched_topk_values(DTYPE[kd], _ptr(keys), _ptr(values), 8, _ptr(segment_offsets),
+                                           num_segments, int(k), DIRECTION[direction],
+                                           DETERMINISM[determinism], TIE_BREAK[tie_break], ORDERING[ordering],
+                                           _ptr(out_keys), _ptr(out_values), ml, ctypes.byref(opts),
+                                           _stream_handle(stream, keys.device))
+    else:
+        rc = L.segtopk_batched_topk_ex(DTYPE[kd], _ptr(keys), _ptr(values), _ptr(segment_offsets),
+                                       num_segments, int(k), DIRECTION[direction],
+                                       DETERMINISM[determinism], TIE_BREAK[tie_break], ORDERING[ordering],
+                                       _ptr(out_keys), _ptr(out_values), ml, ctypes.byref(opts),
+                                       _stream_handle(stream, keys.device))
+    _check(rc, L)
+    return out_keys, out_values
+
+
+def topk(keys: torch.Tensor, k: int, *, values=None, direction: str = "max",
+         determinism: str = "gpu_to_gpu", tie_break: str = "prefer_smaller_index",
+         ordering: str = "stable_sorted", out_keys=None, out_values=None, key_dtype: str | None = None,
+         workspace=None, stream=None, lib=None):
+    """Top-k over one array (segtopk_topk): keys is a 1-D CUDA tensor,
+    values an optional int32 / int64 tensor of the same length. The device
+    workspace is allocated here (as a torch tensor) unless given.
+    Returns (out_keys, out_values) of k slots (out_values None for keys only)."""
+    L = lib if lib is not None else load()
+    kd = key_dtype_of(keys, key_dtype)
+    n = keys.numel()
+    vb = 0 if values is None else values.element_size()
+    if values is not None and values.dtype not in (torch.int32, torch.int64):
+        raise ValueError("values must be int32 or int64")
+    if out_keys is None:
+        out_keys = torch.empty(k, dtype=keys.dtype, device=keys.device)
+    if values is not None and out_values is None:
+        out_values = torch.empty(k, dtype=values.dtype, device=keys.device)
+    need = int(L.segtopk_topk_workspace_bytes(DTYPE[kd], vb, n, int(k)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=keys.device)
+    rc = L.segtopk_topk(DTYPE[kd], _ptr(keys), _ptr(values), vb if vb else 4, n, int(k), DIRECTION[direction],
+                        DETERMINISM[determinism], TIE_BREAK[tie_break], ORDERING[ordering], _ptr(out_keys),
+                        _ptr(out_values), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream, keys.device))
     _check(rc, L)
     return out_keys, out_values
 

@@ -252,9 +252,9 @@ bool valid_pair(int det, int tie)
   return det == SEGTOPK_GPU_TO_GPU;
 }
 
-int validate(int dtype, const void* keys, const int32_t* values, const int64_t* offsets,
+int validate(int dtype, const void* keys, const void* values, const int64_t* offsets,
              int64_t num_segments, int32_t k, int direction, int determinism, int tie_break,
-             int ordering, const void* out_keys, const int32_t* out_values, int64_t max_len,
+             int ordering, const void* out_keys, const void* out_values, int64_t max_len,
              bool index_values = false)
 {
   if (dtype < SEGTOPK_F16 || dtype > SEGTOPK_I32)
@@ -291,11 +291,14 @@ int validate(int dtype, const void* keys, const int32_t* values, const int64_t* 
 // out_values is not: out_values then receives each selected element's
 // segment-local source index (the host-buffer path gathers the values
 // itself).
-int run_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values, const int64_t* segment_offsets,
-             int64_t num_segments, int32_t k, segtopk_direction direction, segtopk_determinism determinism,
-             segtopk_tie_break tie_break, segtopk_ordering ordering, void* out_keys, int32_t* out_values,
-             int64_t max_segment_len, const segtopk_options* options, void* stream, bool index_values)
+int run_topk(segtopk_dtype key_dtype, const void* keys, const void* values, int value_bytes,
+             const int64_t* segment_offsets, int64_t num_segments, int32_t k, segtopk_direction direction,
+             segtopk_determinism determinism, segtopk_tie_break tie_break, segtopk_ordering ordering, void* out_keys,
+             void* out_values, int64_t max_segment_len, const segtopk_options* options, void* stream,
+             bool index_values)
 {
+  if (value_bytes != 4 && value_bytes != 8)
+    return SEGTOPK_ERROR_INVALID_VALUE;
   t_last_launch_count = 0;
   int forced_width = 0;
   int32_t small_max = 0, team_max = 0;
@@ -380,6 +383,7 @@ int run_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values, c
     w.offsets = segment_offsets;
     w.out_keys = out_keys;
     w.out_values = out_values;
+    w.value_bytes = value_bytes;
     w.num_segments = num_segments;
     w.n_lo = lo;
     w.n_hi = std::min<int64_t>(hi, max_len);
@@ -387,6 +391,8 @@ int run_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values, c
     w.k = k;
     w.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;
     w.sorted = (ordering != SEGTOPK_UNSORTED) ? 1 : 0;
+    w.stable = (ordering == SEGTOPK_STABLE_SORTED) ? 1 : 0;
+    w.tie_any = (determinism == SEGTOPK_NOT_GUARANTEED) ? 1 : 0;
     w.flag_overlong = max_len <= hi ? 1 : 0; // longer segments belong to a later launch
     e = ops.launch_warp[team](w, st);
     if (e != cudaSuccess)
@@ -405,6 +411,7 @@ int run_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values, c
   p.offsets = segment_offsets;
   p.out_keys = out_keys;
   p.out_values = out_values;
+  p.value_bytes = value_bytes;
   p.num_segments = num_segments;
   p.n_lo = lim2; // shorter segments took a warp-select path
   p.n_hi = max_len;
@@ -433,6 +440,8 @@ int run_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values, c
   p.test_extra_tx = g_test_extra_tx;
   p.prefer_larger = (tie_break == SEGTOPK_PREFER_LARGER_INDEX) ? 1 : 0;
   p.sorted = (ordering != SEGTOPK_UNSORTED) ? 1 : 0;
+  p.stable = (ordering == SEGTOPK_STABLE_SORTED) ? 1 : 0;
+  p.tie_any = (determinism == SEGTOPK_NOT_GUARANTEED) ? 1 : 0;
   p.flag_overlong = 1;
   e = ops.launch[pl.shape.profile](p, pl.shape, st);
   if (e != cudaSuccess)
@@ -458,8 +467,22 @@ extern "C" int segtopk_batched_topk_ex(segtopk_dtype key_dtype, const void* keys
                                        void* out_keys, int32_t* out_values, int64_t max_segment_len,
                                        const segtopk_options* options, void* stream)
 {
-  return run_topk(key_dtype, keys, values, segment_offsets, num_segments, k, direction, determinism, tie_break,
+  return run_topk(key_dtype, keys, values, 4, segment_offsets, num_segments, k, direction, determinism, tie_break,
                   ordering, out_keys, out_values, max_segment_len, options, stream, false);
+}
+
+extern "C" int segtopk_batched_topk_values(segtopk_dtype key_dtype, const void* keys, const void* values,
+                                           int32_t value_bytes, const int64_t* segment_offsets,
+                                           int64_t num_segments, int32_t k, segtopk_direction direction,
+                                           segtopk_determinism determinism, segtopk_tie_break tie_break,
+                                           segtopk_ordering ordering, void* out_keys, void* out_values,
+                                           int64_t max_segment_len, const segtopk_options* options, void* stream)
+{
+  t_last_launch_count = 0;
+  if (values && value_bytes != 4 && value_bytes != 8)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  return run_topk(key_dtype, keys, values, values ? value_bytes : 4, segment_offsets, num_segments, k, direction,
+                  determinism, tie_break, ordering, out_keys, out_values, max_segment_len, options, stream, false);
 }
 
 extern "C" int segtopk_batched_topk(segtopk_dtype key_dtype, const void* keys, const int32_t* values,
@@ -562,7 +585,7 @@ extern "C" int segtopk_batched_topk_host(segtopk_dtype key_dtype, const void* ke
     e = cudaMemcpyAsync(d_out_idx, out_values, slots * 4, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess)
     return cuda_fail(e);
-  int rc = run_topk(key_dtype, d_keys, nullptr, d_offs, num_segments, k, direction, determinism, tie_break,
+  int rc = run_topk(key_dtype, d_keys, nullptr, 4, d_offs, num_segments, k, direction, determinism, tie_break,
                     ordering, d_out_keys, d_out_idx, max_len, nullptr, stream, true);
   if (rc != SEGTOPK_SUCCESS)
     return rc;
@@ -669,4 +692,129 @@ extern "C" int segtopk_set_test_hooks(long long wait_limit_cycles, uint32_t firs
   g_test_extra_tx = first_copy_extra_bytes;
   return SEGTOPK_SUCCESS;
 #endif
+}
+
+// ---------------------------------------------------------------------------
+// Top-k over one array (no segments): two passes of the segmented selection.
+// Pass 1 splits the array into `pieces` balanced contiguous pieces and
+// writes each piece's k best, stably sorted, into the workspace; pass 2
+// selects the k best of those pieces * k candidates. Every key of the array
+// that is among its k best is among its piece's k best, so pass 2 sees all
+// of them; and since each piece's candidates keep equal keys in source-index
+// order and pieces follow one another in source order, a candidate's
+// position orders equal keys as their array index does -- pass 2's tie-break
+// and stable order are the array's.
+// ---------------------------------------------------------------------------
+namespace segtopk {
+namespace topk_detail {
+// Offsets of pass 1's balanced pieces and of pass 2's single segment.
+__global__ void fill_piece_offsets(int64_t* offs, int64_t pieces, int64_t n, int64_t* offs2, int64_t candidates)
+{
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t q = n / pieces, r = n % pieces;
+  if (i <= pieces)
+    offs[i] = i * q + (i < r ? i : r);
+  if (i == 0) {
+    offs2[0] = 0;
+    offs2[1] = candidates;
+  }
+}
+} // namespace topk_detail
+} // namespace segtopk
+
+namespace {
+
+// Pieces of pass 1 for n keys: each at least max(65536, 16 k) keys, at most
+// 304 of them (one wave of two CTAs on each of the 152 SMs).
+int64_t topk_pieces(int64_t n, int32_t k)
+{
+  const int64_t min_piece = std::max<int64_t>(65536, 16 * (int64_t)k);
+  return std::max<int64_t>(1, std::min<int64_t>(304, n / min_piece));
+}
+
+struct TopkLayout {
+  int64_t pieces;
+  size_t offs, offs2, ckeys, cvals, total;
+};
+
+TopkLayout topk_layout(int dtype, int32_t value_bytes, int64_t n, int32_t k)
+{
+  TopkLayout t;
+  t.pieces = topk_pieces(n, k);
+  const size_t cand = (size_t)t.pieces * (size_t)k;
+  t.offs = 0;
+  t.offs2 = ws_align((size_t)(t.pieces + 1) * 8);
+  t.ckeys = t.offs2 + ws_align(16);
+  t.cvals = t.ckeys + ws_align(cand * (size_t)key_bytes_of(dtype));
+  t.total = t.cvals + (value_bytes ? ws_align(cand * (size_t)value_bytes) : 0);
+  return t;
+}
+
+} // namespace
+
+extern "C" size_t segtopk_topk_workspace_bytes(segtopk_dtype key_dtype, int32_t value_bytes, int64_t num_keys,
+                                               int32_t k)
+{
+  if (num_keys < 0 || k < 0 || (value_bytes != 0 && value_bytes != 4 && value_bytes != 8) ||
+      key_dtype < SEGTOPK_F16 || key_dtype > SEGTOPK_I32)
+    return 0;
+  return topk_layout(key_dtype, value_bytes, num_keys, k).total;
+}
+
+extern "C" int segtopk_topk(segtopk_dtype key_dtype, const void* keys, const void* values, int32_t value_bytes,
+                            int64_t num_keys, int32_t k, segtopk_direction direction,
+                            segtopk_determinism determinism, segtopk_tie_break tie_break,
+                            segtopk_ordering ordering, void* out_keys, void* out_values, void* workspace,
+                            size_t workspace_bytes, void* stream)
+{
+  t_last_launch_count = 0;
+  if (num_keys < 0 || (values && value_bytes != 4 && value_bytes != 8) || (!values != !out_values))
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  const int vb = values ? value_bytes : 4;
+  // the rest of the argument checks are the segmented call's (one segment)
+  int v = validate(key_dtype, keys, values, workspace ? (const int64_t*)workspace : nullptr, 1, k, direction,
+                   determinism, tie_break, ordering, out_keys, out_values, 0);
+  if (v >= 0)
+    return v;
+  if (num_keys == 0)
+    return SEGTOPK_SUCCESS;
+  if (((uintptr_t)workspace & 255u) != 0)
+    return SEGTOPK_ERROR_MISALIGNED;
+  const TopkLayout t = topk_layout(key_dtype, values ? value_bytes : 0, num_keys, k);
+  if (workspace_bytes < t.total)
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  if ((num_keys + t.pieces - 1) / t.pieces > SEGTOPK_MAX_SEGMENT_LEN)
+    return SEGTOPK_ERROR_NOT_SUPPORTED;
+  char* w = (char*)workspace;
+  int64_t* offs = (int64_t*)(w + t.offs);
+  int64_t* offs2 = (int64_t*)(w + t.offs2);
+  void* ckeys = w + t.ckeys;
+  void* cvals = values ? (void*)(w + t.cvals) : nullptr;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int64_t cand = t.pieces * (int64_t)k;
+  segtopk::topk_detail::fill_piece_offsets<<<(unsigned)((t.pieces + 1 + 255) / 256), 256, 0, st>>>(offs, t.pieces, num_keys, offs2, cand);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess)
+    return cuda_fail(e);
+  if (t.pieces == 1) {
+    const int rc = run_topk(key_dtype, keys, values, vb, offs, 1, k, direction, determinism, tie_break, ordering,
+                            out_keys, out_values, num_keys, nullptr, stream, false);
+    if (rc == SEGTOPK_SUCCESS)
+      t_last_launch_count += 1;
+    return rc;
+  }
+  // pass 1: every piece's k best, stably sorted (any order when any ties will do)
+  const segtopk_ordering order1 = determinism == SEGTOPK_NOT_GUARANTEED ? SEGTOPK_UNSORTED : SEGTOPK_STABLE_SORTED;
+  int rc = run_topk(key_dtype, keys, values, vb, offs, t.pieces, k, direction, determinism, tie_break, order1,
+                    ckeys, cvals, (num_keys + t.pieces - 1) / t.pieces, nullptr, stream, false);
+  if (rc != SEGTOPK_SUCCESS)
+    return rc;
+  const int launches1 = t_last_launch_count;
+  // pass 2: the k best of the candidates
+  rc = run_topk(key_dtype, ckeys, cvals, vb, offs2, 1, k, direction, determinism, tie_break, ordering, out_keys,
+                out_values, cand, nullptr, stream, false);
+  if (rc != SEGTOPK_SUCCESS)
+    return rc;
+  t_last_launch_count += launches1 + 1;
+  return SEGTOPK_SUCCESS;
 }

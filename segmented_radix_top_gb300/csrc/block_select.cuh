@@ -32,6 +32,7 @@ struct __align__(16) PassSlot {
   uint32_t ncand;          // candidates stored in the position buffer
   uint32_t kept;           // compaction: entries written so far
   uint32_t nfin;           // counting finish: keys staged
+  uint32_t ties;           // compaction: boundary entries taken by arrival so far
   unsigned long long kmax; // compaction: largest rank written
 };
 
@@ -200,6 +201,7 @@ __device__ __forceinline__ void clear_slot(PassSlot& sl)
     sl.ncand = 0;
     sl.kept = 0;
     sl.nfin = 0;
+    sl.ties = 0;
     sl.kmax = 0;
   }
 }
@@ -402,12 +404,17 @@ __device__ __forceinline__ uint32_t pref_index(uint32_t idx, bool prefer_larger)
 // Which list entries form the k best: (rank & mask) < prefix are strictly
 // better than the boundary ("front"); among the boundary candidates
 // ((rank & mask) == prefix) those with (pref_index & imask) <= iprefix are
-// taken. imask == 0 takes every boundary candidate.
+// taken. imask == 0 takes every boundary candidate -- or, with take > 0,
+// the first `take` of them in order of arrival (a compaction counts them):
+// the tie choice of the not_guaranteed determinism mode, where any subset of
+// the ties is valid ("Top-K: Determinism, Tie-Breaking, and Output
+// Ordering", "Determinism" table).
 template <class Rank>
 struct Selection {
   Rank prefix, mask;
   uint32_t iprefix, imask;
-  uint32_t n; // entries selected
+  uint32_t n;    // entries selected
+  uint32_t take; // > 0: boundary entries taken by arrival, at most this many
   // 0: not selected, 1: front, 2: selected boundary entry
   __device__ __forceinline__ int classify(Rank r, uint32_t pidx) const
   {
@@ -502,7 +509,7 @@ __device__ __forceinline__ void select_ties_ordered(Ctrl& ctl, const Src<typenam
 template <class TR, int NT>
 __device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, uint32_t& pass, const Src<typename TR::Raw>& src,
                                                      uint32_t kk, uint32_t slack, typename TR::Rank dirmask,
-                                                     bool prefer_larger, CandBuf cb)
+                                                     bool prefer_larger, CandBuf cb, bool tie_any)
 {
   using Rank = typename TR::Rank;
   const Radix<Rank> rr = radix_select<Rank, TR::kRankBits, NT>(ctl, pass, src.size(), nullptr, 0u, kk, slack, ~0u, cb,
@@ -515,6 +522,8 @@ __device__ Selection<typename TR::Rank> block_select(Ctrl& ctl, uint32_t& pass, 
     s.n = kk - rr.krem + rr.cnt;
   else if (src.count == 0) // every rank digit resolved, more than krem ties, ring keys only
     select_ties_ordered<TR, NT>(ctl, src, rr.krem, dirmask, prefer_larger, s);
+  else if (tie_any) // more than krem ties and any of them will do: the first to arrive
+    s.take = rr.krem;
   else // every rank digit resolved and more than krem entries share the boundary rank
     select_ties<TR, NT>(ctl, pass, src, rr.krem, dirmask, prefer_larger, s, cb);
   return s;
@@ -679,11 +688,25 @@ __device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, uint32
     Raw kr = 0;
     uint32_t ki = 0;
     Rank rk = 0;
+    int cls = 0;
     if (e < n) {
       kr = src.key(e);
       ki = src.index(e);
       rk = TR::rank(kr, dirmask);
-      keep = s.classify(rk, pref_index(ki, prefer_larger)) != 0;
+      cls = s.classify(rk, pref_index(ki, prefer_larger));
+      keep = cls != 0;
+    }
+    if (s.take) {
+      // boundary entries by arrival: one counter add per warp and round
+      const uint32_t tb = __ballot_sync(kFull, cls == 2);
+      if (tb) {
+        uint32_t tbase = 0;
+        if (lane_id() == 0)
+          tbase = atomicAdd(&sl.ties, __popc(tb));
+        tbase = __shfl_sync(kFull, tbase, 0);
+        if (cls == 2)
+          keep = tbase + __popc(tb & lanemask_lt()) < s.take;
+      }
     }
     const uint32_t bal = __ballot_sync(kFull, keep);
     if (bal) {
@@ -714,10 +737,10 @@ template <class TR, int NT>
 __device__ __forceinline__ Kept<typename TR::Rank> trim_into(Ctrl& ctl, uint32_t pass, const Src<typename TR::Raw> src,
                                                           typename TR::Raw* dst_raw, uint32_t* dst_idx, uint32_t kk,
                                                           uint32_t slack, typename TR::Rank dirmask,
-                                                          bool prefer_larger, CandBuf cb)
+                                                          bool prefer_larger, CandBuf cb, bool tie_any)
 {
   const Selection<typename TR::Rank> s =
-    block_select<TR, NT>(ctl, pass, src, kk, slack, dirmask, prefer_larger, cb);
+    block_select<TR, NT>(ctl, pass, src, kk, slack, dirmask, prefer_larger, cb, tie_any);
   return select_into<TR, NT>(ctl, pass, src, s, dst_raw, dst_idx, kk + slack, dirmask, prefer_larger);
 }
 
@@ -740,6 +763,7 @@ __device__ __forceinline__ Kept<typename TR::Rank> tie_block_into(Ctrl& ctl, uin
     // select_into counts in the slot of the last digit pass; none ran here
     PassSlot& sl = ctl.slot[(pass + 2) % 3];
     sl.kept = 0;
+    sl.ties = 0;
     sl.kmax = 0;
   }
   const uint32_t n = src.ext_count;
@@ -1180,8 +1204,7 @@ __host__ __device__ inline uint32_t finalize_scratch_bytes(uint32_t n) { return 
 template <class TR, int NT>
 __device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, const uint32_t* idx, uint32_t n, uint32_t k,
                                             typename TR::Rank dirmask, bool prefer_larger, bool sorted,
-                                            unsigned char* scratch, typename TR::Raw* out_keys, int32_t* out_values,
-                                            const int32_t* values)
+                                            unsigned char* scratch, typename TR::Raw* out_keys, const ValueSink& vals)
 {
   constexpr int EC = (int)((kCountMax + NT - 1) / NT);
   constexpr bool wide = TR::kRankBits > 32;
@@ -1210,8 +1233,8 @@ __device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, cons
       const uint32_t p = pos[i];
       if (p < m) {
         out_keys[p] = raw[i];
-        if (out_values)
-          out_values[p] = value_at(values, idx[i]);
+        if (vals)
+          vals.put(p, idx[i]);
       }
     }
     return;
@@ -1229,8 +1252,8 @@ __device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, cons
     const uint32_t p = pos[i];
     if (p < m) {
       out_keys[p] = raw[i];
-      if (out_values)
-        out_values[p] = value_at(values, idx[i]);
+      if (vals)
+        vals.put(p, idx[i]);
     }
   }
 }
@@ -1247,8 +1270,7 @@ __device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, cons
 template <class TR, int NT, int EPT>
 __device__ __forceinline__ void sort_write_ept(const typename TR::Raw* raw, const uint32_t* idx, uint32_t m,
                                                typename TR::Rank dirmask, unsigned char* scratch,
-                                               typename TR::Raw* out_keys, int32_t* out_values,
-                                               const int32_t* values)
+                                               typename TR::Raw* out_keys, const ValueSink& vals)
 {
   uint64_t a[EPT], b[EPT];
 #pragma unroll
@@ -1276,8 +1298,8 @@ __device__ __forceinline__ void sort_write_ept(const typename TR::Raw* raw, cons
     if (e < m) {
       const uint32_t slot = (uint32_t)b[r];
       out_keys[e] = raw[slot];
-      if (out_values)
-        out_values[e] = value_at(values, idx[slot]);
+      if (vals)
+        vals.put(e, idx[slot]);
     }
   }
 }
@@ -1285,15 +1307,15 @@ __device__ __forceinline__ void sort_write_ept(const typename TR::Raw* raw, cons
 template <class TR, int NT>
 __device__ __forceinline__ void sort_and_write(const typename TR::Raw* raw, const uint32_t* idx, uint32_t m,
                                                typename TR::Rank dirmask, unsigned char* scratch,
-                                               typename TR::Raw* out_keys, int32_t* out_values,
-                                               const int32_t* values)
+                                               typename TR::Raw* out_keys, const ValueSink& vals,
+                                               bool stable = true)
 {
   static_assert(NT == (int)kSortLanes, "sort scratch is sized for kSortLanes threads");
   const uint32_t n2 = next_pow2(m < 2 ? 2 : m);
   if (n2 <= (uint32_t)NT) {
     // one item per thread: registers and shuffles (measured faster up to 256
     // items; above, the shared-memory network below is)
-    sort_write_ept<TR, NT, 1>(raw, idx, m, dirmask, scratch, out_keys, out_values, values);
+    sort_write_ept<TR, NT, 1>(raw, idx, m, dirmask, scratch, out_keys, vals);
     return;
   }
   if constexpr (TR::kRankBits <= 32) {
@@ -1308,8 +1330,25 @@ __device__ __forceinline__ void sort_and_write(const typename TR::Raw* raw, cons
     for (uint32_t j = threadIdx.x; j < m; j += NT) {
       const uint32_t s = pay[j];
       out_keys[j] = raw[s];
-      if (out_values)
-        out_values[j] = value_at(values, idx[s]);
+      if (vals)
+        vals.put(j, idx[s]);
+    }
+  } else if (!stable) {
+    // sorted but not stable (equal keys in any order): 64-bit ranks sort on
+    // the rank alone, the item's slot as payload
+    uint64_t* key = reinterpret_cast<uint64_t*>(scratch);
+    uint32_t* pay = reinterpret_cast<uint32_t*>(key + n2);
+    for (uint32_t i = threadIdx.x; i < n2; i += NT) {
+      key[i] = i < m ? (uint64_t)TR::rank(raw[i], dirmask) : ~0ull;
+      pay[i] = i;
+    }
+    __syncthreads();
+    bitonic_sort_u64<NT>(key, pay, n2);
+    for (uint32_t j = threadIdx.x; j < m; j += NT) {
+      const uint32_t s = pay[j];
+      out_keys[j] = raw[s];
+      if (vals)
+        vals.put(j, idx[s]);
     }
   } else {
     uint64_t* khi = reinterpret_cast<uint64_t*>(scratch);
@@ -1323,8 +1362,8 @@ __device__ __forceinline__ void sort_and_write(const typename TR::Raw* raw, cons
     for (uint32_t j = threadIdx.x; j < m; j += NT) {
       const uint32_t s = (uint32_t)klo[j];
       out_keys[j] = raw[s];
-      if (out_values)
-        out_values[j] = value_at(values, idx[s]);
+      if (vals)
+        vals.put(j, idx[s]);
     }
   }
 }

@@ -434,13 +434,23 @@ __device__ __forceinline__ void vec_set_key(uint4& v, int j, Raw x) // slot j ho
   }
 }
 
-// The value written for the element at segment-local index i: the payload,
-// or, with no payload array (an internal mode of the host-buffer entry
-// point), the index itself.
-__device__ __forceinline__ int32_t value_at(const int32_t* values, uint32_t i)
-{
-  return values ? values[i] : (int32_t)i;
-}
+// Where a segment's selected values go: out[pos] receives the payload of
+// the element at segment-local index idx -- in[idx] with 4- or 8-byte
+// values, or, with no payload array (an internal mode of the host-buffer
+// entry point), idx itself. A sink with no output (keys only) is false.
+struct ValueSink {
+  void* out;      // this segment's output values (null: keys only)
+  const void* in; // this segment's input values (null: write source indices)
+  int wide;       // 8-byte values
+  __device__ __forceinline__ explicit operator bool() const { return out != nullptr; }
+  __device__ __forceinline__ void put(uint32_t pos, uint32_t idx) const
+  {
+    if (wide)
+      static_cast<int64_t*>(out)[pos] = in ? static_cast<const int64_t*>(in)[idx] : (int64_t)idx;
+    else
+      static_cast<int32_t*>(out)[pos] = in ? static_cast<const int32_t*>(in)[idx] : (int32_t)idx;
+  }
+};
 
 // ---------------------------------------------------------------------------
 // Warp helpers

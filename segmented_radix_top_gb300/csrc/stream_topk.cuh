@@ -56,10 +56,10 @@ using ProfileMany = CtaProfile<3, 4, 2048>;
 
 struct KernelParams {
   const void* keys;
-  const int32_t* values;
+  const void* values;    // int32 or int64 payload (value_bytes), or null
   const int64_t* offsets;
   void* out_keys;
-  int32_t* out_values;
+  void* out_values;
   int64_t num_segments;
   int64_t n_lo;          // this launch serves segments with n_lo < n <= n_hi
   int64_t n_hi;
@@ -77,6 +77,9 @@ struct KernelParams {
   float spec_c;
   int32_t spec_small;    // small targets by warp minimums (exact) rather than digit passes (slack stop)
   long long wait_limit;  // clock cycles after which a wait on a bulk copy gives up
+  int32_t value_bytes;   // 4 or 8
+  int32_t tie_any;       // not_guaranteed: surplus boundary ties may be taken in any order
+  int32_t stable;        // sorted output keeps equal keys in source-index order
   uint32_t test_extra_tx; // instrumented build only: bytes added to a slice's first copy's expected count
 };
 
@@ -175,6 +178,7 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   const Rank dirmask = (Rank)p.dirmask;
   const bool is_max = dirmask != 0;
   const bool fwd = !p.prefer_larger;
+  const bool tie_any = p.tie_any != 0;
   const uint32_t S = p.ring_stages;
 
   // ---- front-loaded shared-memory initialisation ----
@@ -252,7 +256,7 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   // buffer, which becomes the list.
   auto select_union = [&](const Raw* ext, uint32_t idx0, uint32_t n_ext, uint32_t slack) {
     const Kept<Rank> kp = trim_into<TR, NT>(ctl, sel_pass, Src<Raw>{list_raw, list_idx, count, ext, idx0, n_ext},
-                                            spare_raw, spare_idx, k, slack, dirmask, pl, cbuf);
+                                            spare_raw, spare_idx, k, slack, dirmask, pl, cbuf, tie_any);
     sel_pass = kp.pass;
     swap_lists();
     set_bound(kp.max_rank, kp.n);
@@ -657,20 +661,22 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     trim_list(0u);
 
   Raw* out_keys = reinterpret_cast<Raw*>(p.out_keys) + seg * (int64_t)k;
-  int32_t* out_values = p.out_values ? p.out_values + seg * (int64_t)k : nullptr;
-  const int32_t* values = p.values ? p.values + g0 : nullptr;
+  const int64_t vbytes = p.value_bytes;
+  const ValueSink vals{p.out_values ? static_cast<char*>(p.out_values) + seg * (int64_t)k * vbytes : nullptr,
+                       p.values ? static_cast<const char*>(p.values) + g0 * vbytes : nullptr, vbytes == 8 ? 1 : 0};
 
   // The k best of n list entries (any order), written to this segment's
   // output slots: small sets by counting, larger ones by a radix selection
   // and then a sort of the k survivors when the output is sorted.
   auto finish = [&](Raw* raw, uint32_t* idx, uint32_t nn, Raw* sp_raw, uint32_t* sp_idx, unsigned char* scratch) {
     if (nn <= kCountMax) {
-      finalize_small<TR, NT>(raw, idx, nn, k, dirmask, pl, p.sorted != 0, scratch, out_keys, out_values, values);
+      finalize_small<TR, NT>(raw, idx, nn, k, dirmask, pl, p.sorted != 0, scratch, out_keys, vals);
       return;
     }
     uint32_t mm = nn; // every entry is selected when nn <= k
     if (nn > k) {
-      sel_pass = trim_into<TR, NT>(ctl, sel_pass, list_src(raw, idx, nn), sp_raw, sp_idx, k, 0u, dirmask, pl, cbuf).pass;
+      sel_pass =
+        trim_into<TR, NT>(ctl, sel_pass, list_src(raw, idx, nn), sp_raw, sp_idx, k, 0u, dirmask, pl, cbuf, tie_any).pass;
       raw = sp_raw;
       idx = sp_idx;
       mm = k;
@@ -678,13 +684,13 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     if (!p.sorted) {
       for (uint32_t e = threadIdx.x; e < mm; e += NT) {
         out_keys[e] = raw[e];
-        if (out_values)
-          out_values[e] = value_at(values, idx[e]);
+        if (vals)
+          vals.put(e, idx[e]);
       }
     } else if (mm <= kCountMax) {
-      finalize_small<TR, NT>(raw, idx, mm, mm, dirmask, pl, true, scratch, out_keys, out_values, values);
+      finalize_small<TR, NT>(raw, idx, mm, mm, dirmask, pl, true, scratch, out_keys, vals);
     } else {
-      sort_and_write<TR, NT>(raw, idx, mm, dirmask, scratch, out_keys, out_values, values);
+      sort_and_write<TR, NT>(raw, idx, mm, dirmask, scratch, out_keys, vals, p.stable != 0);
     }
   };
 
@@ -868,9 +874,10 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   cluster_sync(); // every CTA's bases are final
   const uint32_t fbase = ctl.front_base, tbase = ctl.tie_base;
 
-  // this CTA's share of the boundary ties, chosen by source index
+  // this CTA's share of the boundary ties, chosen by source index (any of
+  // them in the not_guaranteed mode: the first `quota` in list order)
   const uint32_t quota = ties_needed > tbase ? min(tot.y, ties_needed - tbase) : 0u;
-  if (quota > 0 && quota < tot.y)
+  if (quota > 0 && quota < tot.y && !tie_any)
   {
     CandBuf cb = cbuf;
     cb.n = ~0u;
@@ -888,10 +895,12 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   if (!p.sorted) {
     scan_list<TR, NT>(ctl, lsrc, dirmask, classify,
                       [&](uint32_t, Raw kr, uint32_t ki, Rank, int cls, uint32_t r1, uint32_t r2) {
+                        if (cls == 2 && r2 >= quota)
+                          return; // a surplus tie (not_guaranteed)
                         const uint32_t pos = position(cls, r1, r2);
                         out_keys[pos] = kr;
-                        if (out_values)
-                          out_values[pos] = value_at(values, ki);
+                        if (vals)
+                          vals.put(pos, ki);
                       });
     SEGTOPK_FLUSH_STATS();
     return;
@@ -905,6 +914,8 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   const uint32_t gidx = dsmem_map(smem_addr(g_idx), leader);
   scan_list<TR, NT>(ctl, lsrc, dirmask, classify,
                     [&](uint32_t, Raw kr, uint32_t ki, Rank, int cls, uint32_t r1, uint32_t r2) {
+                      if (cls == 2 && r2 >= quota)
+                        return; // a surplus tie (not_guaranteed)
                       const uint32_t pos = position(cls, r1, r2);
                       dsmem_st(graw + pos * (uint32_t)sizeof(Raw), kr);
                       dsmem_st(gidx + pos * 4u, ki);
@@ -914,7 +925,7 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     SEGTOPK_FLUSH_STATS();
     return;
   }
-  sort_and_write<TR, NT>(g_raw, g_idx, m, dirmask, scratch, out_keys, out_values, values);
+  sort_and_write<TR, NT>(g_raw, g_idx, m, dirmask, scratch, out_keys, vals, p.stable != 0);
   SEGTOPK_FLUSH_STATS();
 #undef SEGTOPK_FLUSH_STATS
 }

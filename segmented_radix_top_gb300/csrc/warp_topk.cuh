@@ -30,7 +30,8 @@
 // Output: the first min(k, n) entries in composite order, which is the
 // stable sorted order (rank, then source index) when smaller indices are
 // preferred; with larger indices preferred the entries are re-sorted by
-// (rank, source index) for sorted output. Key bits are read back from the
+// (rank, source index) for stable sorted output (for sorted output without
+// stability, composite order -- equal keys by descending index -- is kept). Key bits are read back from the
 // segment by source index (so -0.0 keeps its sign), values likewise.
 #pragma once
 
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
 
   // lanes [0, m) hold the selection in composite order
   uint32_t idx = pl ? ~top.pref() : top.pref();
-  if (p.sorted && pl) {
+  if (p.sorted && pl && p.stable) { // (for sorted, not stable, composite order is a valid order)
     OutKey<Rank> o{lane < m ? top.rank() : ~(Rank)0, lane < m ? idx : ~0u};
     o = warp_sort32(o);
     idx = o.i;
@@ -373,8 +374,12 @@ __global__ void __launch_bounds__(32 * W, (W == 1) ? 32 : 4) warp_topk_kernel(co
   if (lane < m) {
     Raw* out_keys = reinterpret_cast<Raw*>(p.out_keys) + seg * (int64_t)k;
     out_keys[lane] = keys[g0 + idx];
-    if (p.out_values)
-      p.out_values[seg * (int64_t)k + lane] = p.values ? p.values[g0 + idx] : (int32_t)idx;
+    if (p.out_values) {
+      const int64_t vb = p.value_bytes;
+      const ValueSink vals{static_cast<char*>(p.out_values) + seg * (int64_t)k * vb,
+                           p.values ? static_cast<const char*>(p.values) + g0 * vb : nullptr, vb == 8 ? 1 : 0};
+      vals.put(lane, idx);
+    }
   }
 }
 

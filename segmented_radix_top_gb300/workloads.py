@@ -184,6 +184,17 @@ def workload5(segments: int = 4096, seg_len: int = 32768, mode: str = "nondet") 
                     "max", det, tie, order)
 
 
+def array_workload(n: int = 1 << 28) -> Workload:
+    """Top-k over one array (no segments): 2^28 fp32 keys ~ N(0,1), k=1024,
+    max, pairs with value = int32 position, gpu_to_gpu + prefer_smaller_index
+    + stable_sorted (one segment covering the whole array)."""
+    g = _rng(1010)
+    x = g.standard_normal(size=n, dtype=np.float32)
+    return Workload("fp32 array of %d N(0,1), k=1024 max pairs (no segments)" % n, "f32", f32_bits(x),
+                    np.arange(n, dtype=np.int32), offsets_from_lengths([n]), 1024, "max", "gpu_to_gpu",
+                    "prefer_smaller_index", "stable_sorted", info={"array": True})
+
+
 def by_number(cfg: int, **kw) -> Workload:
     return {1: workload1, 2: workload2, 3: workload3, 4: workload4, 5: workload5}[cfg](**kw)
 

@@ -215,3 +215,30 @@ def test_too_small_length_hint_is_reported(dtype):
         part = W.Workload("hint", dtype, np.zeros(int(offs[-1]), dtype=wl.keys.dtype), None, offs, k,
                           wl.direction, wl.determinism, wl.tie_break, wl.ordering)
         compare(part, gk, gv, wk, wv, where="%s k=%d C=%d short segments" % (dtype, k, width))
+
+
+@pytest.mark.parametrize("width", [1, 4])
+def test_not_guaranteed_ties_and_unstable_sort(width):
+    """The cheaper variants: not_guaranteed takes surplus boundary ties in any
+    order (no selection by index), sorted without stability sorts 64-bit
+    keys on the key alone. Half of every long segment ties at one value
+    (the k-th key falls inside the tie block), as in the u32 workload;
+    checked by the contract of each mode (multisets, order, real elements)."""
+    g = np.random.Generator(np.random.PCG64(960 + width))
+    lengths = [7, 300, 5000, 70001, 131072]
+    n = sum(lengths)
+    keys = g.integers(0, 2**32, size=n, dtype=np.uint64).astype(np.uint32)
+    keys[g.random(n) < 0.5] = 0xFFC00000
+    offs = W.offsets_from_lengths(lengths)
+    vals = g.integers(-2**31, 2**31, size=n, dtype=np.int64).astype(np.int32)
+    for k, ordering in [(1024, "unsorted"), (1024, "sorted"), (100, "stable_sorted"), (600, "unsorted")]:
+        wl = W.Workload("ties", "u32", keys, vals, offs, k, "max", "not_guaranteed", "unspecified", ordering)
+        check_workload(wl, cluster_width=width, where="u32 ties nondet k=%d %s C=%d" % (k, ordering, width))
+    f = W.random_workload(970 + width, "f64", [600, 3000, 40000, 90001], 600, "max", "gpu_to_gpu",
+                          "prefer_smaller_index", "sorted", pairs=True, distinct=50)
+    check_workload(f, cluster_width=width, where="f64 sorted k=600 C=%d" % width)
+    w = W.random_workload(980 + width, "f16", [33, 500, 4000, 9000], 24, "min", "gpu_to_gpu",
+                          "prefer_larger_index", "sorted", pairs=True, distinct=12)
+    check_workload(w, cluster_width=0, small_segment_max_len=100000, where="f16 warp sorted prefer_larger")
+    check_workload(w, cluster_width=0, team_segment_max_len=100000, small_segment_max_len=-1,
+                   where="f16 team sorted prefer_larger")
