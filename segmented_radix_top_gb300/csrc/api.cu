@@ -69,7 +69,6 @@ cudaError_t device_info(DeviceInfo* out)
   return cudaSuccess;
 }
 
-constexpr uint32_t kStages = 2;
 constexpr int64_t kMinSliceKeys = 16384; // a CTA of a multi-CTA cluster reads at least this many keys
 constexpr int kThreads = kCtaThreads;
 
@@ -93,11 +92,8 @@ constexpr uint32_t kGatherMaxItems = 2048;
 // read) tightens the bound.
 uint32_t list_slack(uint32_t k) { return std::max(1024u, k / 2); }
 
-// Ring bytes of a kernel profile (kStages stages).
-uint32_t profile_ring_bytes(int profile)
-{
-  return kStages * (profile == 0 ? ProfileLong::kChunkBytes : ProfileMany::kChunkBytes);
-}
+// Ring bytes of a kernel profile.
+uint32_t profile_ring_bytes(int profile) { return profile == 0 ? ProfileLong::kRingBytes : ProfileMany::kRingBytes; }
 uint32_t profile_cand_bytes(int profile) { return profile == 0 ? ProfileLong::kCandBytes : ProfileMany::kCandBytes; }
 
 // Wait bound and copy-count offset handed to the kernels (changed only by the
@@ -434,7 +430,6 @@ int run_topk(segtopk_dtype key_dtype, const void* keys, const void* values, int 
   p.spec_small = (pl.waves <= 1 || ops.rank_bits == 64) ? 1 : 0;
   p.spec_z = pl.waves <= 1 ? 4.0f : (p.spec_small ? 3.0f : 2.0f);
   p.spec_c = pl.waves <= 1 ? 3.0f : (p.spec_small ? 2.0f : 1.0f);
-  p.ring_stages = kStages;
   p.ring_bytes = pl.ring_bytes;
   p.wait_limit = g_wait_limit;
   p.test_extra_tx = g_test_extra_tx;

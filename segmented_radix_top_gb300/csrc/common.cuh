@@ -6,6 +6,7 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -203,6 +204,12 @@ __device__ __forceinline__ void dsmem_st(uint32_t addr, uint64_t v)
 // Each key kind provides
 //   rank(x, dirmask)       the rank code (smaller = better);
 //   unrank(r, dirmask)     raw bits of a key with rank r (never -0.0);
+//   pass_bits(v, braw, brank, is_max)
+//                          per key of a 16-byte vector, a bit that is set
+//                          for every key ranking below brank (and may be set
+//                          for NaNs and, for 64-bit keys, keys whose high
+//                          word ties braw's); key_of_bit(q) is the key
+//                          behind bit q;
 //   may_pass(v, braw, brank, is_max, strict)
 //                          for a 16-byte vector of keys: false only if no key
 //                          in it ranks below brank (strict) or at most brank
@@ -243,6 +250,17 @@ struct FloatRank {
   }
 };
 
+// Eight 16-bit lanes' compare masks (0xffff per true half) to one bit per
+// key: bits 0-3 are the low halves of words 0-3 (keys 0, 2, 4, 6), bits 4-7
+// the high halves (keys 1, 3, 5, 7).
+__device__ __forceinline__ uint32_t half_mask_bits(uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3)
+{
+  const uint32_t b = (m0 & 0x00010001u) | ((m1 & 0x00010001u) << 1) | ((m2 & 0x00010001u) << 2) |
+                     ((m3 & 0x00010001u) << 3);
+  return (b & 0xfu) | (b >> 12);
+}
+__device__ __forceinline__ uint32_t half_key_of_bit(uint32_t q) { return q < 4u ? 2u * q : 2u * (q - 4u) + 1u; }
+
 template <>
 struct KeyTraits<KeyKind::F16> {
   using Raw = uint16_t;
@@ -256,6 +274,16 @@ struct KeyTraits<KeyKind::F16> {
   {
     return FloatRank<uint16_t, 16>::t_inv((uint16_t)(r ^ dirmask));
   }
+  __device__ __forceinline__ static uint32_t pass_bits(const uint4& v, Raw braw, Rank, bool is_max)
+  {
+    const __half e = __ushort_as_half(braw);
+    const __half2 h = __halves2half2(e, e);
+    const __half2* w = reinterpret_cast<const __half2*>(&v);
+    if (is_max)
+      return half_mask_bits(__hgtu2_mask(w[0], h), __hgtu2_mask(w[1], h), __hgtu2_mask(w[2], h), __hgtu2_mask(w[3], h));
+    return half_mask_bits(__hltu2_mask(w[0], h), __hltu2_mask(w[1], h), __hltu2_mask(w[2], h), __hltu2_mask(w[3], h));
+  }
+  __device__ __forceinline__ static uint32_t key_of_bit(uint32_t q) { return half_key_of_bit(q); }
   __device__ __forceinline__ static bool may_pass(const uint4& v, Raw braw, Rank, bool is_max, bool strict)
   {
     const __half e = __ushort_as_half(braw);
@@ -285,6 +313,16 @@ struct KeyTraits<KeyKind::BF16> {
   {
     return FloatRank<uint16_t, 16>::t_inv((uint16_t)(r ^ dirmask));
   }
+  __device__ __forceinline__ static uint32_t pass_bits(const uint4& v, Raw braw, Rank, bool is_max)
+  {
+    const __nv_bfloat16 e = __ushort_as_bfloat16(braw);
+    const __nv_bfloat162 h = __halves2bfloat162(e, e);
+    const __nv_bfloat162* w = reinterpret_cast<const __nv_bfloat162*>(&v);
+    if (is_max)
+      return half_mask_bits(__hgtu2_mask(w[0], h), __hgtu2_mask(w[1], h), __hgtu2_mask(w[2], h), __hgtu2_mask(w[3], h));
+    return half_mask_bits(__hltu2_mask(w[0], h), __hltu2_mask(w[1], h), __hltu2_mask(w[2], h), __hltu2_mask(w[3], h));
+  }
+  __device__ __forceinline__ static uint32_t key_of_bit(uint32_t q) { return half_key_of_bit(q); }
   __device__ __forceinline__ static bool may_pass(const uint4& v, Raw braw, Rank, bool is_max, bool strict)
   {
     const __nv_bfloat16 e = __ushort_as_bfloat16(braw);
@@ -311,6 +349,18 @@ struct KeyTraits<KeyKind::F32> {
   {
     return FloatRank<uint32_t, 32>::t_inv(r ^ dirmask);
   }
+  __device__ __forceinline__ static uint32_t pass_bits(const uint4& v, Raw braw, Rank, bool is_max)
+  {
+    const float f = __uint_as_float(braw);
+    const float x0 = __uint_as_float(v.x), x1 = __uint_as_float(v.y);
+    const float x2 = __uint_as_float(v.z), x3 = __uint_as_float(v.w);
+    if (is_max)
+      return (uint32_t)!(x0 <= f) | ((uint32_t)!(x1 <= f) << 1) | ((uint32_t)!(x2 <= f) << 2) |
+             ((uint32_t)!(x3 <= f) << 3);
+    return (uint32_t)!(x0 >= f) | ((uint32_t)!(x1 >= f) << 1) | ((uint32_t)!(x2 >= f) << 2) |
+           ((uint32_t)!(x3 >= f) << 3);
+  }
+  __device__ __forceinline__ static uint32_t key_of_bit(uint32_t q) { return q; }
   __device__ __forceinline__ static bool may_pass(const uint4& v, Raw braw, Rank, bool is_max, bool strict)
   {
     const float f = __uint_as_float(braw);
@@ -345,6 +395,15 @@ struct KeyTraits<KeyKind::F64> {
     const int32_t x = (int32_t)hi;
     return x ^ (int32_t)((uint32_t)(x >> 31) >> 1);
   }
+  __device__ __forceinline__ static uint32_t pass_bits(const uint4& v, Raw braw, Rank, bool is_max)
+  {
+    const int32_t ob = order_hi((uint32_t)(braw >> 32));
+    const int32_t o0 = order_hi(v.y), o1 = order_hi(v.w);
+    if (is_max)
+      return (uint32_t)(o0 >= ob) | ((uint32_t)(o1 >= ob) << 1);
+    return (uint32_t)(o0 <= ob) | ((uint32_t)(o1 <= ob) << 1);
+  }
+  __device__ __forceinline__ static uint32_t key_of_bit(uint32_t q) { return q; }
   __device__ __forceinline__ static bool may_pass(const uint4& v, Raw braw, Rank, bool is_max, bool)
   {
     // a key ranking at most the bound is, as a number, at least (max) or at
@@ -365,6 +424,13 @@ struct KeyTraits<KeyKind::U32> {
   static constexpr int kRankBits = 32;
   __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return x ^ dirmask; }
   __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask) { return r ^ dirmask; }
+  __device__ __forceinline__ static uint32_t pass_bits(const uint4& v, Raw, Rank brank, bool is_max)
+  {
+    const uint32_t dm = is_max ? 0xffffffffu : 0u; // exact
+    return (uint32_t)((v.x ^ dm) < brank) | ((uint32_t)((v.y ^ dm) < brank) << 1) |
+           ((uint32_t)((v.z ^ dm) < brank) << 2) | ((uint32_t)((v.w ^ dm) < brank) << 3);
+  }
+  __device__ __forceinline__ static uint32_t key_of_bit(uint32_t q) { return q; }
   __device__ __forceinline__ static bool may_pass(const uint4& v, Raw, Rank brank, bool is_max, bool strict)
   {
     const uint32_t dm = is_max ? 0xffffffffu : 0u; // exact
@@ -381,6 +447,13 @@ struct KeyTraits<KeyKind::I32> {
   static constexpr int kRankBits = 32;
   __device__ __forceinline__ static Rank rank(Raw x, Rank dirmask) { return (x ^ 0x80000000u) ^ dirmask; }
   __device__ __forceinline__ static Raw unrank(Rank r, Rank dirmask) { return (r ^ dirmask) ^ 0x80000000u; }
+  __device__ __forceinline__ static uint32_t pass_bits(const uint4& v, Raw, Rank brank, bool is_max)
+  {
+    const uint32_t dm = (is_max ? 0xffffffffu : 0u) ^ 0x80000000u; // exact
+    return (uint32_t)((v.x ^ dm) < brank) | ((uint32_t)((v.y ^ dm) < brank) << 1) |
+           ((uint32_t)((v.z ^ dm) < brank) << 2) | ((uint32_t)((v.w ^ dm) < brank) << 3);
+  }
+  __device__ __forceinline__ static uint32_t key_of_bit(uint32_t q) { return q; }
   __device__ __forceinline__ static bool may_pass(const uint4& v, Raw, Rank brank, bool is_max, bool strict)
   {
     const uint32_t dm = (is_max ? 0xffffffffu : 0u) ^ 0x80000000u; // exact

@@ -37,15 +37,19 @@ namespace segtopk {
 constexpr int kCtaThreads = 256;
 
 // A kernel profile: CTAs an SM is sized for, 16-byte vectors a thread filters
-// per ring stage (a stage holds kCtaThreads * VEC_PER_THREAD vectors), and
-// the capacity of the selection's candidate-position buffer.
-template <int CTAS_PER_SM, int VEC_PER_THREAD, uint32_t CAND_CAP>
+// per ring stage (a stage holds kCtaThreads * VEC_PER_THREAD vectors), the
+// capacity of the selection's candidate-position buffer, and the ring's
+// stages (a power of two, so that stage and phase are bit operations).
+template <int CTAS_PER_SM, int VEC_PER_THREAD, uint32_t CAND_CAP, uint32_t STAGES = 2>
 struct CtaProfile {
   static constexpr int kCtasPerSm = CTAS_PER_SM;
   static constexpr int kVecPerThread = VEC_PER_THREAD;
   static constexpr uint32_t kChunkBytes = 16u * (uint32_t)VEC_PER_THREAD * (uint32_t)kCtaThreads;
   static constexpr uint32_t kCandCap = CAND_CAP;
   static constexpr uint32_t kCandBytes = CAND_CAP * 2u;
+  static constexpr uint32_t kStages = STAGES;
+  static constexpr uint32_t kRingBytes = STAGES * kChunkBytes;
+  static_assert(STAGES >= 2 && STAGES <= 8 && (STAGES & (STAGES - 1)) == 0, "ring stages");
 };
 // Long segments served by one wave of CTAs or clusters: two CTAs per SM,
 // 32 KiB stages (fewer, larger chunks per segment).
@@ -66,7 +70,6 @@ struct KernelParams {
   uint64_t dirmask;      // rank = T(key) ^ dirmask: all ones for max, zero for min
   int32_t k;
   uint32_t list_cap;     // candidate list capacity (entries)
-  uint32_t ring_stages;  // pipeline depth (<= 8)
   uint32_t ring_bytes;   // ring region bytes (also sort / gather scratch)
   int32_t prefer_larger; // tie preference: larger source index first
   int32_t sorted;        // write the selected items in stable sorted order
@@ -99,6 +102,7 @@ enum StatIndex : int {
   kStatWaitCycles = 11, // cycles thread 0 spent waiting for copies
   kStatKeys = 12,       // keys of the slices
   kStatSlowChunks = 13, // chunk shares of warp 0 that held candidates
+  kStatFallbackChunks = 14, // chunk offers that overflowed the list
   kStatCount = 16
 };
 
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   const bool is_max = dirmask != 0;
   const bool fwd = !p.prefer_larger;
   const bool tie_any = p.tie_any != 0;
-  const uint32_t S = p.ring_stages;
+  constexpr uint32_t S = PR::kStages;
 
   // ---- front-loaded shared-memory initialisation ----
   for (uint32_t i = threadIdx.x; i < kBuckets; i += NT) {
@@ -266,17 +270,13 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     select_union(nullptr, 0u, 0u, slack);
   };
 
-  // Offer this thread's U vectors (vector j: vc[j] keys from slot 0, source
-  // indices i0[j] + slot). Keys that may beat the bound are tested exactly;
-  // accepted keys are appended at list positions count + (a per-lane atomic
-  // on this step's counter). Returns true if an append would overflow the
-  // list (nothing is written for that lane then).
-  auto offer = [&](const uint4 (&vec)[U], const uint32_t (&vc)[U], const uint32_t (&i0)[U]) {
-    uint32_t mayv = 0;
-#pragma unroll
-    for (int j = 0; j < U; ++j)
-      if (vc[j] && (open || TR::may_pass(vec[j], bound.raw, bound.tau, is_max, true)))
-        mayv |= 1u << j;
+  // Test the flagged vectors exactly (bit j of mayv: vector j, with vc[j]
+  // keys from slot 0 and source indices i0[j] + slot, may hold a key that
+  // beats the bound) and append the accepted keys at list positions count +
+  // (a per-lane atomic on this step's counter). Returns true if an append
+  // would overflow the list (nothing is written for that lane then).
+  auto append_flagged = [&](const uint4 (&vec)[U], const uint32_t (&vc)[U], const uint32_t (&i0)[U],
+                            uint32_t mayv) {
     bool overflow = false;
     if (mayv) {
       uint32_t acc[U];
@@ -318,6 +318,15 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     }
     return overflow;
   };
+  // Offer up to U loose vectors (the edges): every key when no bound is set yet.
+  auto offer = [&](const uint4 (&vec)[U], const uint32_t (&vc)[U], const uint32_t (&i0)[U]) {
+    uint32_t mayv = 0;
+#pragma unroll
+    for (int j = 0; j < U; ++j)
+      if (vc[j] && (open || TR::may_pass(vec[j], bound.raw, bound.tau, is_max, true)))
+        mayv |= 1u << j;
+    return append_flagged(vec, vc, i0, mayv);
+  };
 
   // After a step's barrier: account its appends (unless a selection replaced
   // the list) and recycle the counter of the step before, which every thread
@@ -330,73 +339,51 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
     ++step;
   };
 
-  // Offer a chunk in the ring: every thread filters U vectors (may_pass);
-  // the warp then hands its candidate vectors out one per lane, so a lane
-  // re-reads one flagged vector, tests its keys exactly and appends the
-  // accepted ones. Returns true if an append would overflow the list.
-  auto offer_chunk = [&](const uint4* stage, uint32_t v0, uint32_t v1, uint32_t idx0) {
+  // Candidate bits of this thread's vectors [v0, v1) of a ring stage: bits
+  // j * VK .. j * VK + VK - 1 hold TR::pass_bits of vector j = j * NT +
+  // thread (a superset of the keys ranking below the bound: exact but for
+  // NaNs and, for 64-bit keys, ties of the high words).
+  using CandMask = typename std::conditional<(U * VK > 32), uint64_t, uint32_t>::type;
+  auto candidate_bits = [&](const uint4* stage, uint32_t v0, uint32_t v1) {
     uint4 vv[U];
 #pragma unroll
-    for (int j = 0; j < U; ++j) // all loads first (in the ring; vectors outside [v0, v1) are masked below)
+    for (int j = 0; j < U; ++j) // all loads first (vectors outside [v0, v1) are masked below)
       vv[j] = stage[(uint32_t)j * NT + threadIdx.x];
-    uint32_t mayv = 0;
+    CandMask m = 0;
 #pragma unroll
     for (int j = 0; j < U; ++j) {
       const uint32_t t = (uint32_t)j * NT + threadIdx.x;
-      mayv |= (uint32_t)((t >= v0) & (t < v1) & TR::may_pass(vv[j], bound.raw, bound.tau, is_max, true)) << j;
+      const uint32_t b = TR::pass_bits(vv[j], bound.raw, bound.tau, is_max);
+      m |= (CandMask)((t >= v0 && t < v1) ? b : 0u) << (j * VK);
     }
-    if (!__any_sync(kFull, mayv != 0))
-      return false; // the common case: nothing in this warp's share can enter the list
-    SEGTOPK_STAT_ADD(kStatSlowChunks, 1);
-    const uint32_t lane = lane_id(), warp_base = threadIdx.x & ~31u;
-    uint32_t cand[U], base[U], total = 0;
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      cand[j] = __ballot_sync(kFull, (mayv >> j) & 1u);
-      base[j] = total;
-      total += __popc(cand[j]);
-    }
+    return m;
+  };
+
+  // Test this thread's candidates exactly (rank below the bound), each read
+  // from the stage, and append the accepted ones at list positions count +
+  // (an atomic on this step's counter, one per key). A lane loops over its
+  // own candidates only, so a warp takes as many rounds as its busiest lane
+  // has candidates. Returns true if an append would overflow the list
+  // (that key is not written).
+  auto append_candidates = [&](const Raw* stage_keys, CandMask m, uint32_t idx0) {
     bool overflow = false;
-    for (uint32_t b0 = 0; b0 < total; b0 += 32) {
-      const uint32_t my = b0 + lane;
-      uint32_t acc = 0, i0 = 0;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (my < total) {
-        uint32_t cj = 0, bj = 0, jj = 0;
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-          if (my >= base[j] && my < base[j] + __popc(cand[j])) {
-            cj = cand[j];
-            bj = base[j];
-            jj = (uint32_t)j;
-          }
-        }
-        const uint32_t src_lane = __fns(cj, 0, (int)(my - bj) + 1);
-        const uint32_t t = jj * NT + warp_base + src_lane;
-        v = stage[t];
-        i0 = idx0 + t * VK;
-        const Raw* kv = reinterpret_cast<const Raw*>(&v);
-#pragma unroll
-        for (int i = 0; i < VK; ++i)
-          if (TR::rank(kv[i], dirmask) < bound.tau)
-            acc |= 1u << i;
-      }
-      const uint32_t c = __popc(acc);
-      if (c) {
-        const uint32_t pos = count + atomicAdd(&ctl.chunk_count[step % 3], c);
-        if (pos + c > L) {
-          overflow = true;
+    while (m) {
+      uint32_t q;
+      if constexpr (sizeof(CandMask) == 8)
+        q = (uint32_t)__ffsll((long long)m) - 1u;
+      else
+        q = (uint32_t)__ffs(m) - 1u;
+      m &= m - 1u;
+      const uint32_t j = q / (uint32_t)VK;
+      const uint32_t e = (j * NT + threadIdx.x) * VK + TR::key_of_bit(q % (uint32_t)VK);
+      const Raw key = stage_keys[e];
+      if (TR::rank(key, dirmask) < bound.tau) {
+        const uint32_t pos = count + atomicAdd(&ctl.chunk_count[step % 3], 1u);
+        if (pos < L) {
+          list_raw[pos] = key;
+          list_idx[pos] = idx0 + e;
         } else {
-          const Raw* kv = reinterpret_cast<const Raw*>(&v);
-          uint32_t w = pos;
-#pragma unroll
-          for (int i = 0; i < VK; ++i) {
-            if ((acc >> i) & 1u) {
-              list_raw[w] = kv[i];
-              list_idx[w] = i0 + (uint32_t)i;
-              ++w;
-            }
-          }
+          overflow = true;
         }
       }
     }
@@ -406,25 +393,33 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   // Vectors [v0, v1) of a ring stage: offer them; if the list overflows,
   // trim the list (as it was before the attempt) to tighten the bound and
   // offer them again; if they overflow even a trimmed list, keep the k best
-  // of the list and all of those keys.
-  auto process_vectors = [&](const uint4* stage, uint32_t v0, uint32_t v1, uint32_t idx0) {
+  // of the list and all of those keys. Then the stage is released
+  // (`release` refills it).
+  auto process_vectors = [&](const uint4* stage, uint32_t v0, uint32_t v1, uint32_t idx0, auto&& release) {
     const Raw* stage_keys = reinterpret_cast<const Raw*>(stage);
     bool trimmed = false;
     for (;;) {
-      const bool overflow = offer_chunk(stage, v0, v1, idx0);
+      const CandMask m = candidate_bits(stage, v0, v1);
+      bool overflow = false;
+      if (__any_sync(kFull, m != 0)) { // most warps hold no candidate
+        SEGTOPK_STAT_ADD(kStatSlowChunks, 1);
+        overflow = append_candidates(stage_keys, m, idx0);
+      }
       if (!__syncthreads_or(overflow)) {
         finish_step(true);
-        return;
+        break;
       }
       finish_step(false); // drop this attempt's appends
+      SEGTOPK_STAT_ADD(kStatFallbackChunks, 1);
       if (!trimmed && count > k) {
         trim_list(trim_slack);
         trimmed = true;
       } else {
         select_union(stage_keys + (size_t)v0 * VK, idx0 + v0 * VK, (v1 - v0) * VK, trim_slack);
-        return;
+        break;
       }
     }
+    release();
   };
 
   // Unaligned head / tail keys: plain loads, one per thread.
@@ -505,6 +500,15 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
           landed = s + 1;
         SEGTOPK_STAT_ADD(kStatWaitCycles, clock64() - tw);
       }
+      // refills this stage once every read of it is over (only after this
+      // thread saw every copy so far land, and streaming goes on); once per chunk
+      bool released = false;
+      auto release = [&]() {
+        if (!released && threadIdx.x == 0 && issued < nchunks && landed == s + 1 &&
+            !*reinterpret_cast<volatile uint32_t*>(&ctl.abort))
+          issue_next();
+        released = true;
+      };
       const uint32_t vb = v_lo + chunk_of_step(s) * kChunkVec;
       const uint32_t nv = min(kChunkVec, v_hi - vb);
       const uint4* stage = reinterpret_cast<const uint4*>(ring + (size_t)st * kChunkBytes);
@@ -586,16 +590,12 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
           }
           SEGTOPK_STAT_ADD(kStatFirstBound, clock64() - tb);
           if (nb < nv)
-            process_vectors(stage, fwd ? nb : 0u, fwd ? nv : nv - nb, idx0);
+            process_vectors(stage, fwd ? nb : 0u, fwd ? nv : nv - nb, idx0, release);
         }
       } else {
-        process_vectors(stage, 0u, nv, idx0);
+        process_vectors(stage, 0u, nv, idx0, release);
       }
-      // every read of this stage is over: refill it (only after this
-      // thread saw every copy so far land, and streaming goes on)
-      if (threadIdx.x == 0 && issued < nchunks && landed == s + 1 &&
-          !*reinterpret_cast<volatile uint32_t*>(&ctl.abort))
-        issue_next();
+      release();
     }
     if (threadIdx.x == 0) {
       // after a wait gave up: let every copy still in flight land before
