@@ -352,12 +352,15 @@ SEGTOPK_API int segtopk_last_launch_count(void);
  * segtopk_read_stats: synchronises the device, then sums and clears the
  * per-CTA counters of the segment kernel over every launch since the last
  * read: out[0] CTAs, [1] cycles, [2] cycles to the first bound, [3] cycles
- * of the free-running stream, [4] cycles after it (final selection, merge,
- * output), [5] ring chunks, [6] list trims, [7] slices read twice, [8] list
- * entries at the end of the stream, [9] slices with a sampled first bound,
- * [10] digit-selection passes, [11] cycles warp 0 waited for copies, [12]
- * keys, [13] chunk shares of warp 0 that held candidates; n entries are
- * written (zeros past 15).
+ * of the stream (first bound included), [4] cycles after it (final
+ * selection, merge, output), [5] ring chunks, [6] list trims, [7] slices
+ * read twice, [8] list entries at the end of the stream, [9] slices with a
+ * sampled first bound, [10] digit-selection passes, [11] cycles warp 0
+ * waited for copies, [12] keys, [13] chunk shares of warp 0 that held
+ * candidates, [14] chunk offers that overflowed the list, [15] - [17]
+ * cycles of the small sampled bound's per-warp minimums, merge and write,
+ * [18] / [19] cycles of a lone CTA's final selection and of its output; n
+ * entries are written (zeros past 23).
  *
  * segtopk_set_test_hooks: the bound (SM clock cycles) after which a wait on
  * a bulk copy gives up, and a number of bytes (a multiple of 16, at most

@@ -47,7 +47,8 @@ _lib = None
 _instr = None
 STAT_NAMES = ["ctas", "cycles", "first_bound_cycles", "stream_cycles", "final_cycles", "chunks", "trims",
               "restreams", "list_entries", "sampled_bounds", "digit_passes", "wait_cycles_warp0", "keys",
-              "candidate_shares_warp0"]
+              "candidate_shares_warp0", "overflowing_offers", "spec_warp_cycles", "spec_merge_cycles",
+              "spec_keep_cycles", "final_select_cycles", "final_write_cycles"]
 
 
 def library_path() -> str:
@@ -299,8 +300,8 @@ def read_device_error(lib=None) -> int:
 def read_stats() -> dict:
     """Sums and clears the instrumented build's per-CTA counters (synchronises)."""
     L = load_instrumented()
-    arr = (ctypes.c_uint64 * 16)()
-    _check(L.segtopk_read_stats(arr, 16), L)
+    arr = (ctypes.c_uint64 * len(STAT_NAMES))()
+    _check(L.segtopk_read_stats(arr, len(STAT_NAMES)), L)
     return {name: int(arr[i]) for i, name in enumerate(STAT_NAMES)}
 
 

@@ -39,6 +39,45 @@ struct __align__(16) PassSlot {
 // Keys a warp gathers for the counting finish of a selection.
 constexpr uint32_t kFinishMax = 64;
 
+// Counters of the statistics build (per CTA, summed over the launch).
+enum StatIndex : int {
+  kStatCtas = 0,        // CTAs that served a segment slice
+  kStatCycles = 1,      // clock cycles from start to exit
+  kStatFirstBound = 2,  // cycles spent setting the first bound (sample or exact selection)
+  kStatStream = 3,      // cycles of the stream (first bound included)
+  kStatFinal = 4,       // cycles after the stream: final selection, merge, sort, output
+  kStatChunks = 5,      // ring chunks streamed
+  kStatTrims = 6,       // list trims during the stream
+  kStatRestreams = 7,   // slices read a second time (speculative bound too tight)
+  kStatListEntries = 8, // candidate-list entries at the end of the stream
+  kStatSpec = 9,        // slices whose first bound came from a sample
+  kStatDigitPasses = 10,// digit-selection passes (histogram passes) in the CTA
+  kStatWaitCycles = 11, // cycles thread 0 spent waiting for copies
+  kStatKeys = 12,       // keys of the slices
+  kStatSlowChunks = 13, // chunk shares of warp 0 that held candidates
+  kStatFallbackChunks = 14, // chunk offers that overflowed the list
+  kStatSpecWarp = 15,   // small speculative selection: cycles of the per-warp minimums
+  kStatSpecMerge = 16,  // ... of the merge of the warps' lists
+  kStatSpecKeep = 17,   // ... of writing the kept sample keys
+  kStatFinalSelect = 18,// cycles of a lone CTA's final selection (list to k entries)
+  kStatFinalWrite = 19, // cycles of its output (sort and write)
+  kStatCount = 24
+};
+
+// Adds to a per-CTA counter of the statistics build (thread 0; `ctl` is the
+// CTA's control block); nothing in an ordinary build.
+#ifdef SEGTOPK_STATS
+#define SEGTOPK_STAT_ADD(i, v)                                                                     \
+  do {                                                                                             \
+    if (threadIdx.x == 0)                                                                          \
+      ctl.stat[(i)] += (unsigned long long)(v);                                                    \
+  } while (0)
+#else
+#define SEGTOPK_STAT_ADD(i, v)                                                                     \
+  do {                                                                                             \
+  } while (0)
+#endif
+
 // Control block at the start of dynamic shared memory. Every CTA of a cluster
 // has the same layout, so a field can be addressed in a peer through DSMEM.
 struct Ctrl {
@@ -59,7 +98,7 @@ struct Ctrl {
   uint64_t xb_min[2];                // the cluster-wide minimum of xb
   uint32_t abort;                    // a wait on a bulk copy gave up: the CTA writes no output
   uint32_t pad_;
-  unsigned long long stat[16];       // per-CTA counters of the statistics build
+  unsigned long long stat[kStatCount]; // per-CTA counters of the statistics build
 };
 static_assert(sizeof(PassSlot) % 16 == 0, "every slot's histogram is 16-byte aligned");
 static_assert(offsetof(Ctrl, slot) % 16 == 0, "the slots are 16-byte aligned");
@@ -851,17 +890,20 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_into(Ctrl& ctl, uint32_t
 }
 
 // The speculative first bound for a small target (mm <= 32) and a sample of
-// ring keys only, without digit passes: every thread sorts its (up to 8)
-// sample keys in registers, every warp extracts its mm smallest by repeated
-// warp minimums, and one warp merges the warps' sorted lists the same way;
-// the mm-th smallest is exact because the sample's mm smallest lie among
-// the warps' mm smallest. Selection keys are 32 bits: the rank, or its high
-// word for 64-bit ranks (resolution enough for a first bound). Every sample
-// key at or below the edge is written to dst, as spec_into does; `stage` is
-// 1 KiB of free shared memory. Fails (nothing usable written) on heavy ties
-// at the edge (the target's value also at half the target, or more than
-// 2 mm + 64 keys kept) or an edge at the worst rank.
-template <class TR, int NT>
+// ring keys only (at most KPT per thread), without digit passes: every
+// thread sorts its sample keys in registers, every warp extracts its
+// min(mm, kSpecDepth) smallest by repeated warp minimums, and warp 0 takes
+// the mm-th smallest of the warps' lists, two per lane, the same way. That
+// is the sample's mm-th smallest unless one warp holds more than kSpecDepth
+// of the sample's mm smallest; the edge is then a little worse, and still
+// at least mm sample keys lie at or below it. Selection keys are 32 bits:
+// the rank, or its high word for 64-bit ranks (resolution enough for a first
+// bound). Every sample key at or below the edge is written to dst, as
+// spec_into does; `stage` is 1 KiB of free shared memory. Fails (nothing
+// usable written) on heavy ties at the edge (the target's value also at half
+// the target, or more than 2 mm + 64 keys kept) or an edge at the worst rank.
+constexpr uint32_t kSpecDepth = 8;
+template <class TR, int NT, int KPT>
 __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_t pass, const typename TR::Raw* sample,
                                                               uint32_t idx0, uint32_t ns, uint32_t mm,
                                                               typename TR::Raw* dst_raw, uint32_t* dst_idx,
@@ -869,9 +911,9 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_
                                                               uint32_t* stage)
 {
   using Rank = typename TR::Rank;
-  constexpr int KPT = 8;
   constexpr int NW = NT / 32;
-  static_assert(NW <= 32, "one merge lane per warp");
+  static_assert(NW * kSpecDepth <= 64, "the warps' lists fit two per lane");
+  static_assert(KPT == 4 || KPT == 8, "sample keys per thread");
   auto key32 = [&](uint32_t e) -> uint32_t {
     const Rank r = TR::rank(sample[e], dirmask);
     if constexpr (TR::kRankBits == 64)
@@ -880,6 +922,15 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_
       return (uint32_t)r;
   };
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+#ifdef SEGTOPK_STATS
+  long long t_phase = clock64();
+  auto phase_done = [&](int stat) {
+    SEGTOPK_STAT_ADD(stat, clock64() - t_phase);
+    t_phase = clock64();
+  };
+#else
+  auto phase_done = [](int) {};
+#endif
   uint32_t v[KPT];
 #pragma unroll
   for (int i = 0; i < KPT; ++i) {
@@ -896,36 +947,42 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_
       v[i + 1] = hi;
     }
   }
-  // the warp's mm smallest, in order
-  for (uint32_t it = 0; it < mm; ++it) {
-    const uint32_t mn = __reduce_min_sync(kFull, v[0]);
-    const uint32_t win = __ffs(__ballot_sync(kFull, v[0] == mn)) - 1;
-    if (lane == win) {
+  // the warp's rw smallest, in order (the rest of its list: the worst key)
+  const uint32_t rw = mm < kSpecDepth ? mm : kSpecDepth;
+  for (uint32_t it = 0; it < kSpecDepth; ++it) {
+    uint32_t mn = ~0u;
+    if (it < rw) {
+      mn = __reduce_min_sync(kFull, v[0]);
+      const uint32_t win = __ffs(__ballot_sync(kFull, v[0] == mn)) - 1;
+      if (lane == win) {
 #pragma unroll
-      for (int i = 0; i + 1 < KPT; ++i)
-        v[i] = v[i + 1];
-      v[KPT - 1] = ~0u;
+        for (int i = 0; i + 1 < KPT; ++i)
+          v[i] = v[i + 1];
+        v[KPT - 1] = ~0u;
+      }
     }
     if (lane == 0)
-      stage[warp * 32u + it] = mn;
+      stage[warp * kSpecDepth + it] = mn;
   }
   if (threadIdx.x == 0)
     ctl.spec_kept = 0;
   __syncthreads();
-  // warp 0 merges the NW sorted lists: the mm-th smallest overall
+  phase_done(kStatSpecWarp);
+  // warp 0: the mm-th smallest of the warps' lists (two keys per lane)
   if (warp == 0) {
-    uint32_t p = 0;
-    uint32_t head = lane < (uint32_t)NW ? stage[lane * 32u] : ~0u;
+    const uint32_t x0 = lane < (uint32_t)(NW * kSpecDepth) ? stage[lane] : ~0u;
+    const uint32_t x1 = lane + 32u < (uint32_t)(NW * kSpecDepth) ? stage[lane + 32u] : ~0u;
+    uint32_t lo = min(x0, x1), hi = max(x0, x1);
     uint32_t edge = ~0u, mid = ~0u;
     for (uint32_t it = 0; it < mm; ++it) {
-      const uint32_t mn = __reduce_min_sync(kFull, head);
-      const uint32_t win = __ffs(__ballot_sync(kFull, head == mn)) - 1;
+      const uint32_t mn = __reduce_min_sync(kFull, lo);
+      const uint32_t win = __ffs(__ballot_sync(kFull, lo == mn)) - 1;
       edge = mn;
       if (it == (mm - 1) / 2)
         mid = mn;
       if (lane == win) {
-        ++p;
-        head = p < mm ? stage[lane * 32u + p] : ~0u;
+        lo = hi;
+        hi = ~0u;
       }
     }
     if (lane == 0) {
@@ -934,6 +991,7 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_
     }
   }
   __syncthreads();
+  phase_done(kStatSpecMerge);
   const uint32_t e32 = ctl.res[0];
   if (ctl.res[1]) {
     __syncthreads(); // ctl.res and the stage are free again
@@ -959,6 +1017,7 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_
   __syncthreads();
   const uint32_t kept = ctl.spec_kept;
   __syncthreads(); // ctl.res and the stage are free again
+  phase_done(kStatSpecKeep);
   Rank edge;
   if constexpr (TR::kRankBits == 64)
     edge = ((Rank)e32 << 32) | 0xffffffffull;

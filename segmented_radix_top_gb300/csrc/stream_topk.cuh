@@ -86,40 +86,9 @@ struct KernelParams {
   uint32_t test_extra_tx; // instrumented build only: bytes added to a slice's first copy's expected count
 };
 
-// Counters of the statistics build (per CTA, summed over the launch).
-enum StatIndex : int {
-  kStatCtas = 0,        // CTAs that served a segment slice
-  kStatCycles = 1,      // clock cycles from start to exit
-  kStatFirstBound = 2,  // cycles spent setting the first bound (sample or exact selection)
-  kStatStream = 3,      // cycles of the stream (first bound included)
-  kStatFinal = 4,       // cycles after the stream: final selection, merge, sort, output
-  kStatChunks = 5,      // ring chunks streamed
-  kStatTrims = 6,       // list trims during the stream
-  kStatRestreams = 7,   // slices read a second time (speculative bound too tight)
-  kStatListEntries = 8, // candidate-list entries at the end of the stream
-  kStatSpec = 9,        // slices whose first bound came from a sample
-  kStatDigitPasses = 10,// digit-selection passes (histogram passes) in the CTA
-  kStatWaitCycles = 11, // cycles thread 0 spent waiting for copies
-  kStatKeys = 12,       // keys of the slices
-  kStatSlowChunks = 13, // chunk shares of warp 0 that held candidates
-  kStatFallbackChunks = 14, // chunk offers that overflowed the list
-  kStatCount = 16
-};
-
 // Per-CTA counters of the statistics build, flushed once per CTA.
 static __device__ unsigned long long g_stats[kStatCount];
 
-#ifdef SEGTOPK_STATS
-#define SEGTOPK_STAT_ADD(i, v)                                                                     \
-  do {                                                                                             \
-    if (threadIdx.x == 0)                                                                          \
-      ctl.stat[(i)] += (unsigned long long)(v);                                                    \
-  } while (0)
-#else
-#define SEGTOPK_STAT_ADD(i, v)                                                                     \
-  do {                                                                                             \
-  } while (0)
-#endif
 
 // Host and device agree on the dynamic shared-memory layout.
 __host__ __device__ inline uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -546,8 +515,13 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
               // a small target over ring keys only: warp minimums; else digit passes
               const Spec<Rank> sp =
                 (p.spec_small && count == 0 && mm <= 32u && nbs * VK <= 8u * NT)
-                  ? spec_small<TR, NT>(ctl, sel_pass, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nbs * VK, mm,
-                                       spare_raw, spare_idx, L, dirmask, reinterpret_cast<uint32_t*>(cbuf.pos))
+                  ? (nbs * VK <= 4u * NT
+                       ? spec_small<TR, NT, 4>(ctl, sel_pass, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nbs * VK,
+                                               mm, spare_raw, spare_idx, L, dirmask,
+                                               reinterpret_cast<uint32_t*>(cbuf.pos))
+                       : spec_small<TR, NT, 8>(ctl, sel_pass, stage_keys + (size_t)b0 * VK, idx0 + b0 * VK, nbs * VK,
+                                               mm, spare_raw, spare_idx, L, dirmask,
+                                               reinterpret_cast<uint32_t*>(cbuf.pos)))
                   : spec_into<TR, NT>(ctl, sel_pass,
                                       Src<Raw>{list_raw, list_idx, count, stage_keys + (size_t)b0 * VK,
                                                idx0 + b0 * VK, nbs * VK},
@@ -673,6 +647,9 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
       finalize_small<TR, NT>(raw, idx, nn, k, dirmask, pl, p.sorted != 0, scratch, out_keys, vals);
       return;
     }
+#ifdef SEGTOPK_STATS
+    const long long t_sel = clock64();
+#endif
     uint32_t mm = nn; // every entry is selected when nn <= k
     if (nn > k) {
       sel_pass =
@@ -681,6 +658,15 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
       idx = sp_idx;
       mm = k;
     }
+#ifdef SEGTOPK_STATS
+    const long long t_write = clock64();
+    SEGTOPK_STAT_ADD(kStatFinalSelect, t_write - t_sel);
+    struct WriteTimer {
+      Ctrl& ctl;
+      long long t;
+      __device__ ~WriteTimer() { SEGTOPK_STAT_ADD(kStatFinalWrite, clock64() - t); }
+    } write_timer{ctl, t_write};
+#endif
     if (!p.sorted) {
       for (uint32_t e = threadIdx.x; e < mm; e += NT) {
         out_keys[e] = raw[e];
