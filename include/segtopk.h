@@ -359,8 +359,9 @@ SEGTOPK_API int segtopk_last_launch_count(void);
  * waited for copies, [12] keys, [13] chunk shares of warp 0 that held
  * candidates, [14] chunk offers that overflowed the list, [15] - [17]
  * cycles of the small sampled bound's per-warp minimums, merge and write,
- * [18] / [19] cycles of a lone CTA's final selection and of its output; n
- * entries are written (zeros past 23).
+ * [18] / [19] cycles of a lone CTA's final selection and of its output,
+ * [20] - [22] cycles of every block selection's digit passes, counting
+ * finishes and compactions; n entries are written (zeros past 23).
  *
  * segtopk_set_test_hooks: the bound (SM clock cycles) after which a wait on
  * a bulk copy gives up, and a number of bytes (a multiple of 16, at most

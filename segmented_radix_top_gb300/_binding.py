@@ -48,7 +48,8 @@ _instr = None
 STAT_NAMES = ["ctas", "cycles", "first_bound_cycles", "stream_cycles", "final_cycles", "chunks", "trims",
               "restreams", "list_entries", "sampled_bounds", "digit_passes", "wait_cycles_warp0", "keys",
               "candidate_shares_warp0", "overflowing_offers", "spec_warp_cycles", "spec_merge_cycles",
-              "spec_keep_cycles", "final_select_cycles", "final_write_cycles"]
+              "spec_keep_cycles", "final_select_cycles", "final_write_cycles", "select_pass_cycles",
+              "select_finish_cycles", "select_compact_cycles"]
 
 
 def library_path() -> str:

@@ -61,6 +61,9 @@ enum StatIndex : int {
   kStatSpecKeep = 17,   // ... of writing the kept sample keys
   kStatFinalSelect = 18,// cycles of a lone CTA's final selection (list to k entries)
   kStatFinalWrite = 19, // cycles of its output (sort and write)
+  kStatSelPasses = 20,  // cycles of digit passes of every block selection
+  kStatSelFinish = 21,  // cycles of their counting finishes
+  kStatSelCompact = 22, // cycles of compactions of selected entries
   kStatCount = 24
 };
 
@@ -338,6 +341,9 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t& pass, uint32_t count, co
   uint32_t ncand = 0;
   Key diff = ~(Key)0; // digits that may differ among the remaining candidates
   Key kand_v = 0;
+#ifdef SEGTOPK_STATS
+  long long t_pass = clock64();
+#endif
   for (int p = 0; p < P; ++p) {
     const int shift = KEY_BITS - kDigitBits * (p + 1);
     const Key dmask = (Key)(kBuckets - 1) << shift;
@@ -420,8 +426,16 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t& pass, uint32_t count, co
       // of the pass just done holds the staging counter)
       Key v;
       uint32_t less, eq;
+#ifdef SEGTOPK_STATS
+      SEGTOPK_STAT_ADD(kStatSelPasses, clock64() - t_pass);
+      t_pass = clock64();
+#endif
       finish_by_count<Key, NT>(reinterpret_cast<Key*>(ctl.fin), &ctl.slot[(pass + 2) % 3].nfin, cb.pos, ncand,
                                r.prefix, r.mask, r.krem, get, v, less, eq);
+#ifdef SEGTOPK_STATS
+      SEGTOPK_STAT_ADD(kStatSelFinish, clock64() - t_pass);
+      t_pass = 0;
+#endif
       r.prefix = v;
       r.mask = ~(Key)0;
       r.krem -= less;
@@ -430,6 +444,10 @@ __device__ Radix<Key> radix_select(Ctrl& ctl, uint32_t& pass, uint32_t count, co
       break;
     }
   }
+#ifdef SEGTOPK_STATS
+  if (t_pass)
+    SEGTOPK_STAT_ADD(kStatSelPasses, clock64() - t_pass);
+#endif
   cb.n = compacted ? ncand : ~0u;
   return r;
 }
@@ -721,6 +739,9 @@ __device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, uint32
   PassSlot& sl = ctl.slot[(pass + 2) % 3];
   Rank mx = 0;
   const uint32_t n = src.size();
+#ifdef SEGTOPK_STATS
+  const long long t_compact = clock64();
+#endif
   for (uint32_t base = 0; base < n; base += NT) {
     const uint32_t e = base + threadIdx.x;
     bool keep = false;
@@ -764,6 +785,7 @@ __device__ __forceinline__ Kept<typename TR::Rank> select_into(Ctrl& ctl, uint32
   if (lane_id() == 0 && mx != 0)
     atomicMax(&sl.kmax, (unsigned long long)mx);
   __syncthreads(); // publishes dst and the counters
+  SEGTOPK_STAT_ADD(kStatSelCompact, clock64() - t_compact);
   return Kept<Rank>{(Rank)sl.kmax, s.n < cap ? s.n : cap, pass};
 }
 
