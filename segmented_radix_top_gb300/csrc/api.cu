@@ -110,7 +110,7 @@ Plan size_plan(const KeyOps& ops, int32_t k, int cluster, int profile)
   const uint32_t uk = (uint32_t)k;
   pl.list_cap = align_up(uk + list_slack(uk), 32);
   const uint32_t stream_ring = profile_ring_bytes(profile);
-  const uint32_t sort_need = std::max(sort_scratch_bytes(uk, ops.rank_bits), finalize_scratch_bytes(kCountMax));
+  const uint32_t sort_need = std::max(sort_scratch_bytes(uk, ops.rank_bits), finalize_scratch_bytes(kCountFinalMax));
   uint32_t need = sort_need;
   pl.merge_gather = 0;
   if (cluster > 1) {

@@ -1237,6 +1237,11 @@ __host__ __device__ inline uint32_t sort_scratch_bytes(uint32_t m, int rank_bits
 // far below the fixed cost of digit passes on a few hundred entries.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kCountMax = 128;
+// A lone CTA's final selection takes the counting route up to this many list
+// entries (one per thread: n compares per thread, two barriers), where digit
+// passes and a second selection among boundary ties by source index would
+// each cost a barrier and a histogram.
+constexpr uint32_t kCountFinalMax = 256;
 
 // pos[i] = #{ j < n : key_j < key_i } for unique keys (hi[i], lo[i]) (lo may
 // be null for 64-bit keys). Every thread handles up to EC entries.
@@ -1278,16 +1283,16 @@ __device__ __forceinline__ void count_ranks(const uint64_t* hi, const uint64_t* 
 // Bytes of scratch finalize_small needs for n entries.
 __host__ __device__ inline uint32_t finalize_scratch_bytes(uint32_t n) { return n * (8u + 8u + 4u); }
 
-// The k best of n <= kCountMax list entries, written to one segment's output
+// The k best of n <= MAXN list entries, written to one segment's output
 // slots: unsorted in selection-rank order, or stable sorted by (key, source
 // index). `scratch` holds finalize_scratch_bytes(n) bytes (shared memory);
 // the entries must be visible to the whole block.
-template <class TR, int NT>
+template <class TR, int NT, uint32_t MAXN = kCountMax>
 __device__ __forceinline__ void finalize_small(const typename TR::Raw* raw, const uint32_t* idx, uint32_t n, uint32_t k,
                                             typename TR::Rank dirmask, bool prefer_larger, bool sorted,
                                             unsigned char* scratch, typename TR::Raw* out_keys, const ValueSink& vals)
 {
-  constexpr int EC = (int)((kCountMax + NT - 1) / NT);
+  constexpr int EC = (int)((MAXN + NT - 1) / NT);
   constexpr bool wide = TR::kRankBits > 32;
   uint64_t* kh = reinterpret_cast<uint64_t*>(scratch);
   uint64_t* kl = kh + n;

@@ -643,8 +643,8 @@ __global__ void __launch_bounds__(NT, PR::kCtasPerSm) stream_topk_kernel(const K
   // output slots: small sets by counting, larger ones by a radix selection
   // and then a sort of the k survivors when the output is sorted.
   auto finish = [&](Raw* raw, uint32_t* idx, uint32_t nn, Raw* sp_raw, uint32_t* sp_idx, unsigned char* scratch) {
-    if (nn <= kCountMax) {
-      finalize_small<TR, NT>(raw, idx, nn, k, dirmask, pl, p.sorted != 0, scratch, out_keys, vals);
+    if (nn <= kCountFinalMax) {
+      finalize_small<TR, NT, kCountFinalMax>(raw, idx, nn, k, dirmask, pl, p.sorted != 0, scratch, out_keys, vals);
       return;
     }
 #ifdef SEGTOPK_STATS
