@@ -52,14 +52,19 @@ TEAM_SEGMENT_FEW = 8192
 
 # ----------------------------------------------------------------------------- helpers
 
-def workload_for(name: str):
+def workload_for(name: str, segments=None):
+    """A benchmark workload; `segments` shrinks (or grows) its segment count
+    (for the array workload: its key count), for profiling captures."""
     from segmented_radix_top_gb300 import workloads as W
+    kw = {} if segments is None else {"segments": int(segments)}
     if name == "5det":
-        return W.workload5(mode="det")
+        return W.workload5(mode="det", **kw)
     if name == "5":
-        return W.workload5(mode="nondet")
+        return W.workload5(mode="nondet", **kw)
     if name == "array":
-        return W.array_workload()
+        return W.array_workload(**({} if segments is None else {"n": int(segments)}))
+    if segments is not None:
+        return {"1": W.workload1, "2": W.workload2, "3": W.workload3, "4": W.workload4}[name](**kw)
     return W.by_number(int(name))
 
 
@@ -599,6 +604,24 @@ def run_stats(args):
     return 0
 
 
+def run_profile(args):
+    """Plain (eager) calls of one workload, for ncu captures: no graphs, no
+    host-buffer leg, no CPU baseline. Prints one line and exits."""
+    import torch
+    import segmented_radix_top_gb300 as st
+    name = args.workload or HEADLINE
+    wl = workload_for(name, args.segments)
+    dev = torch.device("cuda", 0)
+    res = Resident(wl, dev, 0)
+    for i in range(args.profile_calls):
+        res.call(i)
+    torch.cuda.synchronize(dev)
+    assert st.read_device_error() == 0
+    print(json.dumps({"profile": name, "workload": wl.name, "calls": args.profile_calls,
+                      "launches_per_call": st.last_launch_count(), "keys": int(wl.lengths.sum())}))
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -609,7 +632,13 @@ def main():
                     help="time one workload only (default: all, workload 5 deterministic as the headline)")
     ap.add_argument("--stats", action="store_true",
                     help="print per-CTA counters of the instrumented build instead of timing")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="make this many plain calls of one workload and exit (ncu captures)")
+    ap.add_argument("--segments", type=int, default=None,
+                    help="with --profile-calls: the workload's segment count (array: key count)")
     args = ap.parse_args()
+    if args.profile_calls > 0:
+        return run_profile(args)
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_setup()
