@@ -397,7 +397,16 @@ struct KeyTraits<KeyKind::F64> {
   }
   __device__ __forceinline__ static uint32_t pass_bits(const uint4& v, Raw braw, Rank, bool is_max)
   {
-    const int32_t ob = order_hi((uint32_t)(braw >> 32));
+    const uint32_t bh = (uint32_t)(braw >> 32);
+    // the usual cases in the raw high words: a bound at or above +0.0 for
+    // max (a better key is positive, and positive doubles order like their
+    // bits as signed integers), a negative bound for min (a better key is
+    // negative, and larger magnitudes have larger unsigned bits)
+    if (is_max && (int32_t)bh >= 0)
+      return (uint32_t)((int32_t)v.y >= (int32_t)bh) | ((uint32_t)((int32_t)v.w >= (int32_t)bh) << 1);
+    if (!is_max && (int32_t)bh < 0)
+      return (uint32_t)(v.y >= bh) | ((uint32_t)(v.w >= bh) << 1);
+    const int32_t ob = order_hi(bh);
     const int32_t o0 = order_hi(v.y), o1 = order_hi(v.w);
     if (is_max)
       return (uint32_t)(o0 >= ob) | ((uint32_t)(o1 >= ob) << 1);
