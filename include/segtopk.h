@@ -373,6 +373,23 @@ SEGTOPK_API int segtopk_last_launch_count(void);
 SEGTOPK_API int segtopk_read_stats(uint64_t* out, int n);
 SEGTOPK_API int segtopk_set_test_hooks(long long wait_limit_cycles, uint32_t first_copy_extra_bytes);
 
+/*
+ * segtopk_test_device_prep (instrumented build; host only, no CUDA call):
+ * replays the per-device launch-preparation decisions the library makes
+ * before every launch, on fresh records, for n launches on device ordinals
+ * devices[i]. A launch of the segment kernel has cluster_widths[i] >= 1 and
+ * smem_bytes[i] of dynamic shared memory; cluster_widths[i] <= 0 denotes a
+ * warp-kernel launch. actions[i] receives the attribute calls that launch
+ * would make, every earlier one taken to have succeeded: bit 0 raises the
+ * shared-memory opt-in, bit 1 allows clusters wider than 8, bit 2 sets the
+ * warp kernel's carveout; ~0 for a device ordinal outside 0..63. Function
+ * attributes belong to each device's copy of a kernel, so each device gets
+ * its own calls. Errors: SEGTOPK_ERROR_INVALID_VALUE for n < 0 or a null
+ * array with n > 0.
+ */
+SEGTOPK_API int segtopk_test_device_prep(int n, const int* devices, const uint32_t* smem_bytes,
+                                         const int* cluster_widths, uint32_t* actions);
+
 #ifdef __cplusplus
 }
 #endif

@@ -114,6 +114,9 @@ def _open(path):
     L.segtopk_read_stats.argtypes = [ctypes.POINTER(ctypes.c_uint64), c_int]
     L.segtopk_set_test_hooks.restype = c_int
     L.segtopk_set_test_hooks.argtypes = [ctypes.c_longlong, ctypes.c_uint32]
+    L.segtopk_test_device_prep.restype = c_int
+    L.segtopk_test_device_prep.argtypes = [c_int, ctypes.POINTER(c_int), ctypes.POINTER(ctypes.c_uint32),
+                                           ctypes.POINTER(c_int), ctypes.POINTER(ctypes.c_uint32)]
     return L
 
 
@@ -311,6 +314,22 @@ def set_test_hooks(wait_limit_cycles: int, first_copy_extra_bytes: int = 0):
     every slice's first copy's expected count (see include/segtopk.h)."""
     L = load_instrumented()
     _check(L.segtopk_set_test_hooks(int(wait_limit_cycles), int(first_copy_extra_bytes)), L)
+
+
+def test_device_prep(launches):
+    """Instrumented build only, no CUDA call: the attribute calls each of a
+    sequence of launches (device, dynamic shared-memory bytes, cluster
+    width; width <= 0 for the warp kernel) would make, per the library's
+    per-device records (bit 0 opt-in, bit 1 wide clusters, bit 2 carveout;
+    see include/segtopk.h)."""
+    L = load_instrumented()
+    n = len(launches)
+    devs = (ctypes.c_int * max(n, 1))(*[int(d) for d, _, _ in launches])
+    smem = (ctypes.c_uint32 * max(n, 1))(*[int(b) for _, b, _ in launches])
+    cl = (ctypes.c_int * max(n, 1))(*[int(c) for _, _, c in launches])
+    out = (ctypes.c_uint32 * max(n, 1))()
+    _check(L.segtopk_test_device_prep(n, devs, smem, cl, out), L)
+    return [int(out[i]) for i in range(n)]
 
 
 def last_launch_count() -> int:

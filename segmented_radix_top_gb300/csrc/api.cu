@@ -9,6 +9,7 @@
 
 #include "../../include/segtopk.h"
 #include "block_select.cuh"
+#include "device_prep.h"
 #include "dispatch.h"
 #include "stream_topk.cuh"
 #include "warp_topk.cuh"
@@ -685,6 +686,42 @@ extern "C" int segtopk_set_test_hooks(long long wait_limit_cycles, uint32_t firs
     return SEGTOPK_ERROR_INVALID_VALUE;
   g_wait_limit = wait_limit_cycles;
   g_test_extra_tx = first_copy_extra_bytes;
+  return SEGTOPK_SUCCESS;
+#endif
+}
+
+extern "C" int segtopk_test_device_prep(int n, const int* devices, const uint32_t* smem_bytes,
+                                        const int* cluster_widths, uint32_t* actions)
+{
+#ifndef SEGTOPK_TEST_HOOKS
+  (void)n;
+  (void)devices;
+  (void)smem_bytes;
+  (void)cluster_widths;
+  (void)actions;
+  return SEGTOPK_ERROR_NOT_SUPPORTED;
+#else
+  if (n < 0 || (n > 0 && (!devices || !smem_bytes || !cluster_widths || !actions)))
+    return SEGTOPK_ERROR_INVALID_VALUE;
+  // one fresh record per kernel kind, every attribute call taken to succeed
+  DevicePrep stream_rec, warp_rec;
+  for (int i = 0; i < n; ++i) {
+    const int dev = devices[i];
+    if (!DevicePrep::valid(dev)) {
+      actions[i] = ~0u;
+      continue;
+    }
+    if (cluster_widths[i] <= 0) { // a warp-kernel launch
+      const uint32_t need = warp_rec.warp_needs(dev);
+      if (need)
+        warp_rec.warp_done(dev);
+      actions[i] = need;
+    } else {
+      const uint32_t need = stream_rec.stream_needs(dev, smem_bytes[i], cluster_widths[i]);
+      stream_rec.stream_done(dev, smem_bytes[i], need);
+      actions[i] = need;
+    }
+  }
   return SEGTOPK_SUCCESS;
 #endif
 }

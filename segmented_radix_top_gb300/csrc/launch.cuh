@@ -3,23 +3,12 @@
 
 #include <mutex>
 
+#include "device_prep.h"
 #include "dispatch.h"
 #include "stream_topk.cuh"
 #include "warp_topk.cuh"
 
 namespace segtopk {
-
-// Per-device launch preparation of one kernel: the dynamic shared-memory
-// opt-in granted so far and the non-portable cluster permission. Function
-// attributes belong to each device's copy of a kernel, so they are tracked
-// per device ordinal, under a lock.
-struct DevicePrep {
-  static constexpr int kMaxDevices = 64;
-  std::mutex mu;
-  uint32_t granted[kMaxDevices] = {};
-  bool nonportable[kMaxDevices] = {};
-  bool prepared[kMaxDevices] = {};
-};
 
 template <KeyKind KK, int NT, class PR>
 struct StreamLauncher {
@@ -32,21 +21,22 @@ struct StreamLauncher {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
       return e;
-    if (dev < 0 || dev >= DevicePrep::kMaxDevices)
+    if (!DevicePrep::valid(dev))
       return cudaErrorInvalidDevice;
     auto fn = stream_topk_kernel<KK, NT, PR>;
     std::lock_guard<std::mutex> lk(st.mu);
-    if (smem > st.granted[dev]) {
+    const uint32_t need = st.stream_needs(dev, smem, cluster);
+    if (need & DevicePrep::kRaiseSmem) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess)
         return e;
-      st.granted[dev] = smem;
+      st.stream_done(dev, smem, DevicePrep::kRaiseSmem);
     }
-    if (cluster > 8 && !st.nonportable[dev]) {
+    if (need & DevicePrep::kNonPortable) {
       e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess)
         return e;
-      st.nonportable[dev] = true;
+      st.stream_done(dev, smem, DevicePrep::kNonPortable);
     }
     return cudaSuccess;
   }
@@ -117,16 +107,16 @@ struct WarpLauncher {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
       return e;
-    if (dev < 0 || dev >= DevicePrep::kMaxDevices)
+    if (!DevicePrep::valid(dev))
       return cudaErrorInvalidDevice;
     {
       std::lock_guard<std::mutex> lk(st.mu);
-      if (!st.prepared[dev]) {
+      if (st.warp_needs(dev) & DevicePrep::kCarveout) {
         e = cudaFuncSetAttribute(warp_topk_kernel<KK, W>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
           return e;
-        st.prepared[dev] = true;
+        st.warp_done(dev);
       }
     }
     cudaLaunchConfig_t cfg = {};

@@ -86,6 +86,29 @@ def test_diagnostics_are_off_in_the_ordinary_build(lib):
     arr = (ctypes.c_uint64 * 16)()
     assert lib.segtopk_read_stats(arr, 16) == 3
     assert lib.segtopk_set_test_hooks(1000, 16) == 3
+    one = (ctypes.c_int * 1)(0)
+    assert lib.segtopk_test_device_prep(1, one, (ctypes.c_uint32 * 1)(1024), one, (ctypes.c_uint32 * 1)()) == 3
+
+
+def test_launch_preparation_is_kept_per_device():
+    # function attributes belong to each device's copy of a kernel: a second
+    # GPU in the same process needs its own opt-in, wide-cluster permission
+    # and carveout, however far the first one was raised
+    seq = [(0, 50000, 1),    # raise device 0's opt-in
+           (1, 50000, 1),    # device 1 needs its own
+           (0, 40000, 2),    # already granted on device 0
+           (0, 90000, 16),   # a larger opt-in and clusters wider than 8
+           (1, 90000, 16),   # both again on device 1
+           (1, 90000, 16),   # nothing left to do
+           (1, 60000, 12),   # smaller, and wide clusters already allowed
+           (0, 0, 0),        # warp kernel on device 0: carveout once
+           (0, 0, 0),
+           (3, 0, -1),       # and on device 3
+           (64, 1024, 1),    # ordinals outside 0..63 are refused
+           (-1, 1024, 1)]
+    got = B.test_device_prep(seq)
+    assert got == [1, 1, 0, 3, 3, 0, 0, 4, 0, 4, 0xFFFFFFFF, 0xFFFFFFFF]
+    assert B.test_device_prep([]) == []
 
 
 def test_status_strings(lib):
