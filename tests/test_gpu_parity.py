@@ -105,6 +105,28 @@ def test_adversarial_orders(pattern, tie):
                 pattern, tie, direction, k, width))
 
 
+@pytest.mark.parametrize("tie", ["prefer_smaller_index", "prefer_larger_index"])
+def test_f64_bounds_on_either_side_of_zero(tie):
+    """f64 keys whose bound lies below +0.0 for max or at or above it for
+    min (the candidate test's general path), and ordered runs across zero
+    whose bound changes sign during the stream."""
+    g = np.random.Generator(np.random.PCG64(3100))
+    n = 70000
+    neg = -np.abs(g.standard_normal(n) * 50.0) - 1e-3         # all negative
+    pos = np.abs(g.standard_normal(n) * 50.0)                 # all non-negative, with ties at +0.0
+    pos[::997] = 0.0
+    pos[::1009] = -0.0
+    ramp = np.linspace(-1000.0, 1000.0, n)                     # ascending through zero
+    x = np.concatenate([neg, pos, ramp, ramp[::-1], neg[:5000] * 1e-300]).astype(np.float64)
+    lengths = [n, n, n, n, 5000]
+    i = np.arange(x.size, dtype=np.int32)
+    for direction, k in itertools.product(["max", "min"], [1, 50, 700]):
+        wl = W.Workload("f64 signs", "f64", W.f64_bits(x), i, W.offsets_from_lengths(lengths), k,
+                        direction, "gpu_to_gpu", tie, "stable_sorted")
+        for width in (1, 3):
+            check_workload(wl, cluster_width=width, where="f64 signs %s %s k=%d C=%d" % (tie, direction, k, width))
+
+
 def test_offsets_edge_cases():
     """Decreasing offsets (empty), a zero-length batch of segments, n == k,
     n == k + 1, every segment shorter than k."""
