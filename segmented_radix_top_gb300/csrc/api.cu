@@ -418,8 +418,10 @@ int run_topk(segtopk_dtype key_dtype, const void* keys, const void* values, int 
   p.merge_gather = pl.merge_gather;
   // Speculative-bound sample: with one wave the slowest CTA sets the time, so
   // a larger sample (a steadier bound); with many waves the mean matters, so
-  // a smaller one (less selection work per segment).
-  p.spec_keys = pl.waves <= 1 ? 2048u : 1024u;
+  // a smaller one (less selection work per segment), except for 64-bit keys,
+  // whose warp-minimum selection takes the larger sample at little extra
+  // cost and keeps the candidate list about a fifth shorter.
+  p.spec_keys = (pl.waves <= 1 || ops.rank_bits == 64) ? 2048u : 1024u;
   // Its margin, in standard deviations of the sample's share of the k best:
   // a slice whose bound proves too tight is read twice, which with one wave
   // sets the kernel's time (wide margin) and with many waves is averaged out

@@ -990,13 +990,31 @@ __device__ __forceinline__ Spec<typename TR::Rank> spec_small(Ctrl& ctl, uint32_
     ctl.spec_kept = 0;
   __syncthreads();
   phase_done(kStatSpecWarp);
-  // warp 0: the mm-th smallest of the warps' lists (two keys per lane)
+  // warp 0: the mm-th smallest of the warps' lists (two keys per lane, slots
+  // lane and lane + 32): a larger target by counting -- a key's place in the
+  // order (key, slot) is the number of keys before it, 64 independent
+  // comparisons -- a small one by repeated warp minimums
   if (warp == 0) {
     const uint32_t x0 = lane < (uint32_t)(NW * kSpecDepth) ? stage[lane] : ~0u;
     const uint32_t x1 = lane + 32u < (uint32_t)(NW * kSpecDepth) ? stage[lane + 32u] : ~0u;
     uint32_t lo = min(x0, x1), hi = max(x0, x1);
     uint32_t edge = ~0u, mid = ~0u;
-    for (uint32_t it = 0; it < mm; ++it) {
+    if (mm >= 16u) {
+      uint32_t r0 = 0, r1 = 0;
+#pragma unroll 8
+      for (uint32_t j = 0; j < 32; ++j) {
+        const uint32_t y0 = __shfl_sync(kFull, x0, j), y1 = __shfl_sync(kFull, x1, j);
+        r0 += (uint32_t)(y0 < x0 || (y0 == x0 && j < lane)) + (uint32_t)(y1 < x0);
+        r1 += (uint32_t)(y0 <= x1) + (uint32_t)(y1 < x1 || (y1 == x1 && j < lane));
+      }
+      auto at_place = [&](uint32_t q) {
+        const uint32_t b0 = __ballot_sync(kFull, r0 == q), b1 = __ballot_sync(kFull, r1 == q);
+        return b0 ? __shfl_sync(kFull, x0, __ffs(b0) - 1) : __shfl_sync(kFull, x1, __ffs(b1) - 1);
+      };
+      edge = at_place(mm - 1);
+      mid = at_place((mm - 1) / 2);
+    }
+    for (uint32_t it = 0; mm < 16u && it < mm; ++it) {
       const uint32_t mn = __reduce_min_sync(kFull, lo);
       const uint32_t win = __ffs(__ballot_sync(kFull, lo == mn)) - 1;
       edge = mn;
