@@ -7,7 +7,8 @@ newer than the library.
 The instrumented variant (libsegtopk_instr.so, variant="instr") is the same
 sources compiled with SEGTOPK_STATS and SEGTOPK_TEST_HOOKS: per-CTA counters
 (segtopk_read_stats) and the test hooks of the bounded copy wait
-(segtopk_set_test_hooks). It is built only when asked for.
+(segtopk_set_test_hooks). build_all() compiles both in one pool of
+compiler processes.
 """
 from __future__ import annotations
 
@@ -64,33 +65,52 @@ def up_to_date(variant: str = "") -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None, variant: str = "") -> str:
-    build_dir, out_path, variant_flags = VARIANTS[variant]
-    if not force and up_to_date(variant):
-        return out_path
-    os.makedirs(build_dir, exist_ok=True)
-    flags = NVCC_FLAGS + variant_flags + list(extra_flags or [])
+def _compile(variant: str, src: str, extra_flags, verbose: bool) -> str:
+    build_dir, _, variant_flags = VARIANTS[variant]
+    obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + variant_flags + list(extra_flags or []) + ["-c", src, "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
+    if verbose and (r.stdout or r.stderr):
+        sys.stderr.write(r.stdout + r.stderr)
+    return obj
 
-    def compile_one(src):
-        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc()] + ARCH + flags + ["-c", src, "-o", obj]
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, r.stdout, r.stderr))
-        if verbose and (r.stdout or r.stderr):
-            sys.stderr.write(r.stdout + r.stderr)
-        return obj
 
-    srcs = _sources()
-    with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_one, srcs))
+def _link(variant: str, objs) -> str:
+    out_path = VARIANTS[variant][1]
     tmp = out_path + ".tmp.%d" % os.getpid()
-    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
+    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + list(objs)
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
     os.replace(tmp, out_path)
     return out_path
+
+
+def build_variants(variants, force: bool = False, verbose: bool = False, extra_flags=None):
+    """Builds the given variants, every translation unit of all of them in
+    one pool of compiler processes; returns the library paths."""
+    todo = [v for v in variants if force or not up_to_date(v)]
+    for v in todo:
+        os.makedirs(VARIANTS[v][0], exist_ok=True)
+    srcs = _sources()
+    jobs = [(v, s) for v in todo for s in srcs]
+    if jobs:
+        with ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
+            objs = list(ex.map(lambda j: _compile(j[0], j[1], extra_flags, verbose), jobs))
+        for v in todo:
+            _link(v, [o for (vv, _), o in zip(jobs, objs) if vv == v])
+    return [lib_path(v) for v in variants]
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=None, variant: str = "") -> str:
+    return build_variants([variant], force=force, verbose=verbose, extra_flags=extra_flags)[0]
+
+
+def build_all(force: bool = False, verbose: bool = False):
+    """The library and its instrumented variant."""
+    return build_variants(list(VARIANTS), force=force, verbose=verbose)
 
 
 if __name__ == "__main__":
